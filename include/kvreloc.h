@@ -1,0 +1,214 @@
+/*
+ * kvreloc.h -- C ABI of the GB300 (sm_103a) KV relocation / splice / patch library.
+ *
+ * The library moves rows of a paged, bf16 KV cache on one GPU:
+ *   - kv_relocate  copies cached rows into new slots.  The position-free part
+ *                  of each row (the MLA latent c_KV, or the GQA V) is copied
+ *                  verbatim; the RoPE part (MLA k_pe, or every head of the GQA
+ *                  K) is rotated in closed form by R(δ), δ = p_target - p_source.
+ *                  [Irminsul: MLA-native position-independent cache, §2.1 and
+ *                  §2.2; Kamera: unified position-invariant KV cache, §2]
+ *   - kv_splice    applies one Leyline directive D = (s_start, s_end, R, m) per
+ *                  sequence: writes the prefilled stub R at s_start and shifts
+ *                  every downstream row by Δ = |R| - |S| in place, rotating its
+ *                  RoPE part by R(Δ).  [Leyline: KV-cache directives for agentic
+ *                  inference, §2.1 directive, §2.2 δ-rotation, §2.3 integration]
+ *   - kv_patch     adds Kamera's rank-m conditioning patch U_m V_mᵀ to stored
+ *                  rows; the same patch can be fused into kv_relocate.
+ *                  [Kamera §2: KV^(B|A) = R(δ)·KV(B|∅) + U_m V_mᵀ]
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pointers named d_* and every pointer inside kv_pool_desc / kv_patch_desc
+ *    are DEVICE pointers; h_* pointers are host memory.
+ *  - The caller owns all memory.  The library allocates nothing: its scratch
+ *    state lives in the caller's workspace (size from kv_workspace_size()).
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *    Argument errors are reported synchronously, before anything is enqueued,
+ *    and then nothing is modified.  Errors found on the device (an index
+ *    outside its pool or table, a bounded wait that ran out) are recorded in
+ *    the workspace status word and read with kv_get_device_status(); the
+ *    offending rows are skipped, nothing outside the pools is touched, and no
+ *    kernel traps.
+ *  - One workspace serves one call at a time: calls that share a workspace
+ *    must be ordered (same stream, or synchronised).
+ *  - Rotation convention: "rotate-half".  On a rotary vector of d elements,
+ *    pair j is (x[j], x[j+d/2]), j < d/2, with frequency θ_j = base^(-2j/d);
+ *    R(δ) turns pair j by the angle δ·θ_j:
+ *       y[j] = x[j]·cos - x[j+d/2]·sin,  y[j+d/2] = x[j]·sin + x[j+d/2]·cos.
+ *    The angle and its cosine/sine are formed in fp64 (one small table per
+ *    call); the rotation runs in fp32 registers with compensated products and
+ *    one round-to-nearest-even to bf16.  R(0) is the identity, bit for bit.
+ *  - Layout: element e of the copy part of slot s in layer l is the bf16 at
+ *       copy_base + l*copy_layer_stride + s*copy_slot_stride + e   (elements)
+ *    and element (head h, i) of the rotary part is at
+ *       rot_base + l*rot_layer_stride + s*rot_slot_stride + h*rot_head_dim + i.
+ *    An MLA pool of rows c_KV[512] ‖ k_pe[64] is described by
+ *    copy_base = pool, rot_base = pool + 512, both slot strides 576.
+ *    Logical position p of request (or sequence) q is slot
+ *       block_tables[q*max_blocks + p/block_size]*block_size + p%block_size.
+ *  - Alignment: copy_base, rot_base and every stride must give 16-byte aligned
+ *    rows (strides multiples of 8 elements); copy_dim % 8 == 0;
+ *    rot_head_dim % 16 == 0.  Patch factors: 16-byte aligned, strides
+ *    multiples of 4 floats, rank a multiple of 4.
+ */
+#ifndef KVRELOC_H
+#define KVRELOC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st *kv_stream_t;
+
+typedef enum {
+    KV_OK = 0,
+    KV_ERR_INVALID_ARG = 1,  /* null pointer, bad shape, stride, alignment or directive */
+    KV_ERR_OUT_OF_RANGE = 2, /* (device) a slot, block id or request index outside its pool/table */
+    KV_ERR_CAPACITY = 3,     /* kv_splice: block table row too short for seq_len + Δ */
+    KV_ERR_WORKSPACE = 4,    /* workspace NULL, misaligned or smaller than needed */
+    KV_ERR_TIMEOUT = 5,      /* (device) a bounded inter-block wait ran out */
+    KV_ERR_CUDA = 6,         /* a CUDA runtime call failed */
+    KV_ERR_UNSUPPORTED = 7   /* a layout the kernels do not handle */
+} kv_status;
+
+/* Leyline directive modes (Leyline §2.1). */
+typedef enum {
+    KV_AMORTIZE = 0, /* splice in place, shift + rotate downstream rows */
+    KV_FORGET = 1    /* move nothing; truncate to s_start for a re-prefill */
+} kv_mode;
+
+/* One paged KV pool (device memory, bf16 elements, strides in elements). */
+typedef struct {
+    int32_t num_layers;        /* L */
+    int32_t block_size;        /* tokens per paged block (64 in the benchmarks) */
+    int64_t num_slots;         /* slots per layer; a multiple of block_size */
+    void *copy_base;           /* verbatim part: MLA c_KV, or GQA V */
+    int64_t copy_layer_stride;
+    int64_t copy_slot_stride;
+    int32_t copy_dim;          /* 512 (MLA) or H*D (GQA) */
+    void *rot_base;            /* rotated part: MLA k_pe, or GQA K */
+    int64_t rot_layer_stride;
+    int64_t rot_slot_stride;
+    int32_t rot_heads;         /* 1 (MLA) or H (GQA) */
+    int32_t rot_head_dim;      /* 64 (MLA) or 128 (GQA) */
+    double rope_base;          /* 10000, 500000, ... */
+} kv_pool_desc;
+
+/* Rank-m patch factors, one (U, V) pair per channel: index 0 patches the
+ * copy part, index 1 the rotated part; a NULL u or v leaves that channel
+ * unpatched (the same arrays may serve both channels).  fp32:
+ *   U(l, t, r)      = u[l*u_layer_stride + t*u_tok_stride + r]
+ *   V(l, c, col, r) = v[l*v_layer_stride + c*v_chunk_stride + col*v_col_stride + r]
+ * t is the token's index in the call (tok_off[c] + offset in chunk c), col the
+ * column inside the channel (rotated part: head*rot_head_dim + i).  Each
+ * patched value becomes rnd(x + Σ_r U(l,t,r)·V(l,c,col,r)), x the copied or
+ * (fused into kv_relocate) the unrounded rotated value.  An MLA patch over
+ * the 576-wide row is one factor pair: u[0] = u[1], v[1] = v[0] + 512*v_col_stride. */
+typedef struct {
+    int32_t rank; /* m: 4..64, a multiple of 4 */
+    const float *u[2];
+    int64_t u_layer_stride[2];
+    int64_t u_tok_stride[2];
+    const float *v[2];
+    int64_t v_layer_stride[2];
+    int64_t v_chunk_stride[2];
+    int64_t v_col_stride[2];
+} kv_patch_desc;
+
+/* Bytes of device workspace needed by any call on `pool` that moves at most
+ * `max_rows` rows per layer in total (relocate/patch: tokens; splice:
+ * downstream rows plus stub rows over all sequences of the call) and has at
+ * most `max_units` chunks (relocate, patch) or sequences (splice).  The
+ * workspace must be 256-byte aligned.  Returns 0 for an invalid pool. */
+size_t kv_workspace_size(const kv_pool_desc *pool, int64_t max_rows, int32_t max_units);
+
+/* Gather chunks of cached rows from `src` into `dst` (Irminsul §2.2, Kamera §2).
+ * Chunk c covers tokens t = d_tok_off[c] .. d_tok_off[c+1]-1 (d_tok_off has
+ * num_chunks+1 non-decreasing entries, d_tok_off[0] = 0,
+ * d_tok_off[num_chunks] = total_tokens).  Token t is read from source slot
+ * d_src_slots[t] and written to logical position d_chunk_dst_pos[c] +
+ * (t - d_tok_off[c]) of request d_chunk_req[c] in d_block_tables
+ * ([num_reqs][max_blocks] int32).  Its copy part is copied verbatim; each
+ * rotary head is turned by R(d_delta[c]).  `patch` (NULL = none) adds the
+ * rank-m patch before the single rounding.
+ * src and dst may be the same pool when no destination slot is also a source
+ * slot (the call is not in place; overlapping slots give undefined rows).
+ * Shapes (num_layers, copy_dim, rot_heads, rot_head_dim, rope_base) of src
+ * and dst must match. */
+kv_status kv_relocate(const kv_pool_desc *src, const kv_pool_desc *dst, int32_t num_chunks,
+                      int64_t total_tokens, const int32_t *d_tok_off, const int32_t *d_src_slots,
+                      const int32_t *d_chunk_req, const int32_t *d_chunk_dst_pos,
+                      const int32_t *d_delta, const int32_t *d_block_tables, int32_t num_reqs,
+                      int32_t max_blocks, const kv_patch_desc *patch, void *d_workspace,
+                      size_t workspace_bytes, kv_stream_t stream);
+
+/* Apply one directive per sequence, in place (Leyline §2.1-§2.3).
+ * Sequence q uses block-table row q of d_block_tables ([num_seqs][max_blocks]),
+ * has h_seq_lens[q] tokens and the directive
+ *   (h_s_start[q], h_s_end[q], R = h_stub_len[q] prefilled rows, mode)
+ * with 0 <= s_start <= s_end <= seq_len (half-open span S = [s_start, s_end)).
+ * The stub rows of all sequences are stored back to back, in sequence order:
+ *   d_stub_copy [L][Σ h_stub_len][copy_dim],
+ *   d_stub_rot  [L][Σ h_stub_len][rot_heads*rot_head_dim]
+ * (contiguous bf16, 16-byte aligned; may be NULL when Σ h_stub_len = 0).
+ * AMORTIZE: rows [0, s_start) stay; the stub is written verbatim at
+ * [s_start, s_start+|R|); the row at s_end+k moves to s_end+Δ+k with its
+ * copy part verbatim and its rotary part turned by R(Δ), Δ = |R| - |S|;
+ * h_seq_lens[q] becomes seq_len + Δ.  Slots at or beyond the new length keep
+ * whatever they held.  Needs ceil(max(seq_len, seq_len+Δ)/block_size) <=
+ * max_blocks (else KV_ERR_CAPACITY); the caller owns the blocks of every
+ * entry used, distinct across the whole call.  The in-place shift is
+ * overlap-safe for Δ of either sign.
+ * FORGET: moves nothing and sets h_seq_lens[q] = s_start (the caller
+ * re-prefills from there); no device work.
+ * h_seq_lens is updated when the call returns KV_OK (the data movement itself
+ * completes in stream order). */
+kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d_block_tables,
+                    int32_t max_blocks, int32_t *h_seq_lens, const int32_t *h_s_start,
+                    const int32_t *h_s_end, const int32_t *h_stub_len, const void *d_stub_copy,
+                    const void *d_stub_rot, kv_mode mode, void *d_workspace,
+                    size_t workspace_bytes, kv_stream_t stream);
+
+/* Add the rank-m patch to stored rows in place (Kamera §2), one rounding per
+ * value.  Chunks are described as in kv_relocate: the tokens of chunk c sit
+ * at logical positions d_chunk_dst_pos[c] + i of request d_chunk_req[c]. */
+kv_status kv_patch(const kv_pool_desc *pool, int32_t num_chunks, int64_t total_tokens,
+                   const int32_t *d_tok_off, const int32_t *d_chunk_req,
+                   const int32_t *d_chunk_dst_pos, const int32_t *d_block_tables,
+                   int32_t num_reqs, int32_t max_blocks, const kv_patch_desc *patch,
+                   void *d_workspace, size_t workspace_bytes, kv_stream_t stream);
+
+/* Wait for `stream`, then return the device status of the last call that
+ * used this workspace (KV_OK, KV_ERR_OUT_OF_RANGE or KV_ERR_TIMEOUT), or
+ * KV_ERR_CUDA if the synchronisation or the read failed. */
+kv_status kv_get_device_status(const void *d_workspace, kv_stream_t stream);
+
+/* Upper bound, in nanoseconds, of every inter-block wait inside kv_splice
+ * (default 2e9).  Values <= 0 restore the default.  Process-wide. */
+void kv_set_wait_limit_ns(int64_t limit_ns);
+
+/* Run the bounded wait used by kv_splice on a workspace flag that nothing
+ * sets, with the given limit; the device status afterwards is
+ * KV_ERR_TIMEOUT.  Exercises the failure path without faulting a GPU. */
+kv_status kv_check_wait_timeout(void *d_workspace, size_t workspace_bytes, int64_t limit_ns,
+                                kv_stream_t stream);
+
+/* Number of kernels the most recent successful call on this thread enqueued. */
+int32_t kv_last_launch_count(void);
+
+/* Short English name of a status code (static storage). */
+const char *kv_status_string(kv_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t kv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVRELOC_H */

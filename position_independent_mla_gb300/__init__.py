@@ -1,0 +1,247 @@
+"""Python binding of ``libkvreloc.so`` -- GB300 KV relocation / splice / patch.
+
+Argument marshalling only: every step of the data path runs in the CUDA
+kernels behind the C ABI (``include/kvreloc.h``).  PyTorch provides device
+memory and streams.  There is no CPU fallback: if the compiled library is
+missing, importing the binding's entry points raises.
+
+    kv_relocate(src, dst, ...)   gather + R(δ) rotation (+ fused rank-m patch)
+    kv_splice(pool, ...)         in-place Leyline AMORTIZE / FORGET directive
+    kv_patch(pool, ...)          in-place rank-m patch U_m V_mᵀ
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+KV_OK, KV_ERR_INVALID_ARG, KV_ERR_OUT_OF_RANGE, KV_ERR_CAPACITY = 0, 1, 2, 3
+KV_ERR_WORKSPACE, KV_ERR_TIMEOUT, KV_ERR_CUDA, KV_ERR_UNSUPPORTED = 4, 5, 6, 7
+KV_AMORTIZE, KV_FORGET = 0, 1
+
+LIB_PATH = _build.LIB
+
+
+class KVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class kv_pool_desc(C.Structure):
+    _fields_ = [
+        ("num_layers", C.c_int32),
+        ("block_size", C.c_int32),
+        ("num_slots", C.c_int64),
+        ("copy_base", C.c_void_p),
+        ("copy_layer_stride", C.c_int64),
+        ("copy_slot_stride", C.c_int64),
+        ("copy_dim", C.c_int32),
+        ("rot_base", C.c_void_p),
+        ("rot_layer_stride", C.c_int64),
+        ("rot_slot_stride", C.c_int64),
+        ("rot_heads", C.c_int32),
+        ("rot_head_dim", C.c_int32),
+        ("rope_base", C.c_double),
+    ]
+
+
+class kv_patch_desc(C.Structure):
+    _fields_ = [
+        ("rank", C.c_int32),
+        ("u", C.c_void_p * 2),
+        ("u_layer_stride", C.c_int64 * 2),
+        ("u_tok_stride", C.c_int64 * 2),
+        ("v", C.c_void_p * 2),
+        ("v_layer_stride", C.c_int64 * 2),
+        ("v_chunk_stride", C.c_int64 * 2),
+        ("v_col_stride", C.c_int64 * 2),
+    ]
+
+
+_lib: Optional[C.CDLL] = None
+
+
+def load(build_if_missing: bool = False) -> C.CDLL:
+    """The loaded library.  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        if not build_if_missing:
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        _build.build()
+    lib = C.CDLL(LIB_PATH)
+    vp, i32, i64, sz = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
+    P, PP = C.POINTER(kv_pool_desc), C.POINTER(kv_patch_desc)
+    sig = {
+        "kv_workspace_size": (sz, [P, i64, i32]),
+        "kv_relocate": (i32, [P, P, i32, i64, vp, vp, vp, vp, vp, vp, i32, i32, PP, vp, sz, vp]),
+        "kv_splice": (i32, [P, i32, vp, i32, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]),
+        "kv_patch": (i32, [P, i32, i64, vp, vp, vp, vp, i32, i32, PP, vp, sz, vp]),
+        "kv_get_device_status": (i32, [vp, vp]),
+        "kv_set_wait_limit_ns": (None, [i64]),
+        "kv_check_wait_timeout": (i32, [vp, sz, i64, vp]),
+        "kv_last_launch_count": (i32, []),
+        "kv_status_string": (C.c_char_p, [i32]),
+        "kv_version": (i32, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().kv_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    """Device address of a tensor; raw addresses (int / c_void_p) pass through."""
+    if t is None:
+        return None
+    if isinstance(t, torch.Tensor):
+        return t.data_ptr()
+    return t.value if isinstance(t, C.c_void_p) else int(t)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        if not torch.cuda.is_available():
+            return None  # host-side argument checks need no stream
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != KV_OK:
+        raise KVError(status, where)
+
+
+# ---------------------------------------------------------------------------
+# Descriptors
+# ---------------------------------------------------------------------------
+
+def pool_desc(copy: torch.Tensor, rot: torch.Tensor, block_size: int, rot_heads: int,
+              rope_base: float) -> kv_pool_desc:
+    """Describe a pool from two bf16 views: ``copy`` [L][slots][copy_dim] and
+    ``rot`` [L][slots][rot_heads*head_dim] (any strides with a unit last stride;
+    e.g. the two column ranges of one fused [L][slots][576] MLA tensor)."""
+    assert copy.dtype == torch.bfloat16 and rot.dtype == torch.bfloat16
+    assert copy.dim() == 3 and rot.dim() == 3 and copy.stride(2) == 1 and rot.stride(2) == 1
+    assert copy.shape[:2] == rot.shape[:2]
+    L, S, cd = copy.shape
+    return kv_pool_desc(L, block_size, S, copy.data_ptr(), copy.stride(0), copy.stride(1), cd,
+                        rot.data_ptr(), rot.stride(0), rot.stride(1), rot_heads,
+                        rot.shape[2] // rot_heads, float(rope_base))
+
+
+def patch_desc(rank: int, u: Sequence[Optional[torch.Tensor]],
+               v: Sequence[Optional[torch.Tensor]]) -> kv_patch_desc:
+    """Factors per channel (0 = verbatim part, 1 = rotated part): ``u[ch]``
+    fp32 (L, tokens, rank), ``v[ch]`` fp32 (L, chunks, columns, rank), any
+    strides with a unit last stride; None = channel not patched."""
+    d = kv_patch_desc()
+    d.rank = rank
+    for ch in range(2):
+        if u[ch] is None or v[ch] is None:
+            continue
+        uu, vv = u[ch], v[ch]
+        assert uu.dtype == torch.float32 and vv.dtype == torch.float32
+        assert uu.stride(2) == 1 and vv.stride(3) == 1
+        d.u[ch] = uu.data_ptr()
+        d.u_layer_stride[ch] = uu.stride(0)
+        d.u_tok_stride[ch] = uu.stride(1)
+        d.v[ch] = vv.data_ptr()
+        d.v_layer_stride[ch] = vv.stride(0)
+        d.v_chunk_stride[ch] = vv.stride(1)
+        d.v_col_stride[ch] = vv.stride(2)
+    return d
+
+
+# ---------------------------------------------------------------------------
+# Entry points (same names as the C ABI)
+# ---------------------------------------------------------------------------
+
+def kv_workspace_size(pool: kv_pool_desc, max_rows: int, max_units: int) -> int:
+    return int(load().kv_workspace_size(C.byref(pool), int(max_rows), int(max_units)))
+
+
+def workspace(pool: kv_pool_desc, max_rows: int, max_units: int, device="cuda") -> torch.Tensor:
+    """A device workspace (uint8, 256-byte aligned) for calls on ``pool``."""
+    n = kv_workspace_size(pool, max_rows, max_units)
+    if n == 0:
+        raise KVError(KV_ERR_INVALID_ARG, "kv_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def kv_relocate(src: kv_pool_desc, dst: kv_pool_desc, num_chunks: int, total_tokens: int,
+                tok_off, src_slots, chunk_req, chunk_dst_pos, delta, block_tables,
+                num_reqs: int, max_blocks: int, patch: Optional[kv_patch_desc],
+                ws: torch.Tensor, stream=None, check: bool = True) -> int:
+    st = load().kv_relocate(
+        C.byref(src), C.byref(dst), int(num_chunks), int(total_tokens), _ptr(tok_off),
+        _ptr(src_slots), _ptr(chunk_req), _ptr(chunk_dst_pos), _ptr(delta), _ptr(block_tables),
+        int(num_reqs), int(max_blocks), C.byref(patch) if patch is not None else None,
+        ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
+    if check:
+        _check(st, "kv_relocate")
+    return st
+
+
+def kv_splice(pool: kv_pool_desc, num_seqs: int, block_tables, max_blocks: int,
+              seq_lens, s_start, s_end, stub_len, stub_copy, stub_rot, mode: int,
+              ws: Optional[torch.Tensor], stream=None, check: bool = True) -> int:
+    """``seq_lens`` is a host int32 tensor updated in place; ``s_start``,
+    ``s_end``, ``stub_len`` host int32 tensors; stubs device bf16 tensors."""
+    for t in (seq_lens, s_start, s_end, stub_len):
+        assert t.device.type == "cpu" and t.dtype == torch.int32 and t.is_contiguous()
+    st = load().kv_splice(
+        C.byref(pool), int(num_seqs), _ptr(block_tables), int(max_blocks), seq_lens.data_ptr(),
+        s_start.data_ptr(), s_end.data_ptr(), stub_len.data_ptr(), _ptr(stub_copy),
+        _ptr(stub_rot), int(mode), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+        _stream(stream))
+    if check:
+        _check(st, "kv_splice")
+    return st
+
+
+def kv_patch(pool: kv_pool_desc, num_chunks: int, total_tokens: int, tok_off, chunk_req,
+             chunk_dst_pos, block_tables, num_reqs: int, max_blocks: int,
+             patch: kv_patch_desc, ws: torch.Tensor, stream=None, check: bool = True) -> int:
+    st = load().kv_patch(
+        C.byref(pool), int(num_chunks), int(total_tokens), _ptr(tok_off), _ptr(chunk_req),
+        _ptr(chunk_dst_pos), _ptr(block_tables), int(num_reqs), int(max_blocks),
+        C.byref(patch), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
+    if check:
+        _check(st, "kv_patch")
+    return st
+
+
+def kv_get_device_status(ws: torch.Tensor, stream=None) -> int:
+    return int(load().kv_get_device_status(ws.data_ptr(), _stream(stream)))
+
+
+def kv_set_wait_limit_ns(limit_ns: int) -> None:
+    load().kv_set_wait_limit_ns(int(limit_ns))
+
+
+def kv_check_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> int:
+    return int(load().kv_check_wait_timeout(ws.data_ptr(), ws.numel() * ws.element_size(),
+                                            int(limit_ns), _stream(stream)))
+
+
+def kv_last_launch_count() -> int:
+    return int(load().kv_last_launch_count())
+
+
+def kv_version() -> int:
+    return int(load().kv_version())

@@ -1,0 +1,219 @@
+// kv_device.cuh -- device-side building blocks of the KV relocation library
+// (sm_103a).  Row movement is HBM-bound: every row is read once and written
+// once with 16-byte vector accesses; the rotary part is turned in fp32
+// registers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kv_internal.h"
+
+namespace kvr {
+
+// ---------------------------------------------------------------------------
+// 16-byte global accesses
+// ---------------------------------------------------------------------------
+
+// Streaming (evict-first) read and write of KV rows: each byte is touched once.
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    return __ldcs(reinterpret_cast<const uint4 *>(p));
+}
+
+__device__ __forceinline__ void st_stream(void *p, uint4 v)
+{
+    __stcs(reinterpret_cast<uint4 *>(p), v);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 arithmetic helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ bool bf16_finite(uint32_t h) { return (h & 0x7F80u) != 0x7F80u; }
+
+// Error-free sum: s + e == a + b exactly (Knuth's two-sum).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = a + b;
+    float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// Round the value hi + lo (|lo| at most half an fp32 ulp of hi) to the
+// nearest bf16, ties to even.  hi alone decides unless it sits exactly on a
+// bf16 tie; then the sign of lo says on which side the value lies.  NaN
+// becomes the canonical quiet NaN 0x7FC0.
+__device__ __forceinline__ uint32_t bf16_round(float hi, float lo)
+{
+    uint32_t u = __float_as_uint(hi);
+    if ((u & 0x7F800000u) == 0x7F800000u)
+        return (u & 0x007FFFFFu) ? 0x7FC0u : (u >> 16);
+    uint32_t keep = u >> 16, low = u & 0xFFFFu;
+    bool up;
+    if (low != 0x8000u)
+        up = low > 0x8000u;
+    else if (lo != 0.0f)
+        up = (__float_as_uint(lo) >> 31) == (u >> 31);
+    else
+        up = keep & 1u;
+    return keep + (up ? 1u : 0u);
+}
+
+// ---------------------------------------------------------------------------
+// The rotation R(δ) of one (x, y) = (x[j], x[j+d/2]) pair
+// ---------------------------------------------------------------------------
+//
+// The δ-table stores, per (unit, frequency j), cos(δθ_j) = c1 + c2 and
+// sin(δθ_j) = s1 + s2, formed in fp64; c1 and s1 carry at most 16
+// significant bits, so with bf16 inputs (8 bits) the products x*c1 and y*s1
+// are exact in fp32 and fmaf(x, c1, -y*s1) rounds the true difference once.
+// The c2/s2 terms add the next 24 bits.  (hi, lo) then holds the rotated
+// value to about 2^-40 of |x|+|y|, and one tie-aware rounding gives the
+// bf16 nearest to it.
+
+// Output of this lane for one pair: `first` selects x*cos - y*sin (the lane
+// holding the first half of the head) or x*sin + y*cos (second half).
+// `add` is an fp32 term (the rank-m patch, or 0) added before rounding.
+__device__ __forceinline__ uint32_t rotate_one(uint32_t xb, uint32_t yb, float4 cs, bool first,
+                                               float add)
+{
+    const float x = __uint_as_float(xb << 16), y = __uint_as_float(yb << 16);
+    float hi, lo;
+    if (bf16_finite(xb) && bf16_finite(yb)) {
+        float t, u;
+        if (first) {
+            t = fmaf(x, cs.x, -(y * cs.z));
+            u = fmaf(x, cs.y, -(y * cs.w));
+        } else {
+            t = fmaf(x, cs.z, y * cs.x);
+            u = fmaf(x, cs.w, y * cs.y);
+        }
+        two_sum(t, u, hi, lo);
+    } else {
+        // Inf / NaN inputs: plain IEEE arithmetic, as the fp64 definition does
+        const float c = cs.x + cs.y, s = cs.z + cs.w;
+        hi = first ? (x * c - y * s) : (x * s + y * c);
+        lo = 0.0f;
+    }
+    float s, e;
+    two_sum(hi, lo + add, s, e);
+    return bf16_round(s, e);
+}
+
+// x + add, rounded once (patch on a verbatim value).
+__device__ __forceinline__ uint32_t add_round(uint32_t xb, float add)
+{
+    const float x = __uint_as_float(xb << 16);
+    float s, e;
+    two_sum(x, add, s, e);
+    return bf16_round(s, e);
+}
+
+// Rotate one 16-byte vector (8 bf16) of a head.  `mine` is this lane's
+// vector, `other` its partner's (the same 8 frequencies in the other half),
+// `first` tells whether `mine` lies in the first half.  cs points at the 8
+// table entries of these frequencies; add[8] is the patch term (or zeros).
+__device__ __forceinline__ uint4 rotate_vec(uint4 mine, uint4 other, bool first,
+                                            const float4 *cs, const float *add)
+{
+    const uint32_t m[4] = {mine.x, mine.y, mine.z, mine.w};
+    const uint32_t o[4] = {other.x, other.y, other.z, other.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t xw = first ? m[k] : o[k];
+        const uint32_t yw = first ? o[k] : m[k];
+        const uint32_t r0 = rotate_one(xw & 0xFFFFu, yw & 0xFFFFu, cs[2 * k], first, add[2 * k]);
+        const uint32_t r1 = rotate_one(xw >> 16, yw >> 16, cs[2 * k + 1], first, add[2 * k + 1]);
+        out[k] = r0 | (r1 << 16);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__device__ __forceinline__ uint4 add_vec(uint4 x, const float *add)
+{
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        out[k] = add_round(w[k] & 0xFFFFu, add[2 * k]) |
+                 (add_round(w[k] >> 16, add[2 * k + 1]) << 16);
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__device__ __forceinline__ uint4 shfl_xor_u4(uint4 v, int mask)
+{
+    v.x = __shfl_xor_sync(0xFFFFFFFFu, v.x, mask);
+    v.y = __shfl_xor_sync(0xFFFFFFFFu, v.y, mask);
+    v.z = __shfl_xor_sync(0xFFFFFFFFu, v.z, mask);
+    v.w = __shfl_xor_sync(0xFFFFFFFFu, v.w, mask);
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// Status word and bounded waits
+// ---------------------------------------------------------------------------
+
+// First error wins; later ones are dropped.
+__device__ __forceinline__ void set_status(uint32_t *status, uint32_t code)
+{
+    atomicCAS(status, 0u, code);
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Spin until *flag != 0, for at most limit_ns of wall time and at most a
+// fixed number of polls (the poll cap bounds the wait even if the timer
+// misbehaves).  Returns false if the wait ran out.
+static __device__ __noinline__ bool wait_flag(const uint32_t *flag, int64_t limit_ns)
+{
+    const uint64_t t0 = global_ns();
+    const uint64_t max_polls = (uint64_t)limit_ns / 16u + 4096u;
+    unsigned sleep_ns = 32;
+    for (uint64_t it = 0; it < max_polls; ++it) {
+        if (ld_acquire(flag) != 0u)
+            return true;
+        if ((int64_t)(global_ns() - t0) > limit_ns)
+            return false;
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 2048)
+            sleep_ns <<= 1;
+    }
+    return ld_acquire(flag) != 0u;
+}
+
+// Physical slot of logical position pos in a block-table row, or -1 when
+// the position or the block id falls outside the table or the pool.
+__device__ __forceinline__ int64_t slot_of(const int32_t *bt_row, int32_t max_blocks,
+                                           int32_t block, int64_t num_blocks, int64_t pos)
+{
+    if (pos < 0)
+        return -1;
+    const int64_t b = pos / block;
+    if (b >= max_blocks)
+        return -1;
+    const int64_t blk = bt_row[b];
+    if (blk < 0 || blk >= num_blocks)
+        return -1;
+    return blk * block + pos % block;
+}
+
+} // namespace kvr

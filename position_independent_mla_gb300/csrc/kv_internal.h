@@ -1,0 +1,99 @@
+// kv_internal.h -- launch parameters shared by the host entry points and the
+// kernels.  Not part of the public ABI (include/kvreloc.h is).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace kvr {
+
+constexpr int kThreads = 256;         // threads per row-moving block
+constexpr int kMaxSeqsPerLaunch = 64; // splice directives carried in one launch
+constexpr int kMaxRank = 64;          // largest patch rank
+constexpr int kHeaderBytes = 256;     // workspace header: status word, ticket counter
+constexpr int kTileMla = 32;          // rows per tile for MLA rows (576 bf16)
+constexpr int kTileGqa = 16;          // rows per tile for 8 x 128 GQA rows
+
+// Device status codes (same values as kv_status).
+enum : uint32_t { kStatusOk = 0, kStatusOutOfRange = 2, kStatusTimeout = 5 };
+
+// A pool as the kernels see it: byte addresses and byte strides.
+struct PoolView {
+    char *copy;
+    int64_t copy_ls, copy_ss;
+    char *rot;
+    int64_t rot_ls, rot_ss;
+    int64_t num_slots;
+    int64_t num_blocks;
+    int32_t block;
+    int32_t num_layers;
+};
+
+struct PatchView {
+    int32_t m;
+    const float *u[2];
+    int64_t u_ls[2], u_ts[2];
+    const float *v[2];
+    int64_t v_ls[2], v_cs[2], v_cols[2];
+};
+
+// kv_relocate (in_place = 0) and kv_patch (in_place = 1: rows are read from
+// and written back to the destination slots, without rotation).
+struct RelocParams {
+    PoolView src, dst;
+    int32_t num_chunks;
+    int64_t total_tokens;
+    const int32_t *tok_off;
+    const int32_t *src_slots;
+    const int32_t *chunk_req;
+    const int32_t *chunk_dst_pos;
+    const int32_t *delta;
+    const int32_t *block_tables;
+    int32_t num_reqs, max_blocks;
+    const float4 *table; // [num_chunks][head_dim/2]
+    PatchView patch;
+    int32_t patched;
+    int32_t in_place;
+    uint32_t *status;
+};
+
+// Host-side plan of one sequence of a splice launch.
+struct SpliceSeq {
+    int32_t s_start, s_end, seq_len, n_r;
+    int32_t delta;   // n_r - (s_end - s_start)
+    int32_t n_shift; // shift tiles (each covers all layers)
+    int32_t n_stub;  // stub tiles
+    int32_t bt_row;  // block-table row
+    int64_t ticket_base;
+    int64_t flag_base; // flags of this sequence: [n_shift][L]
+    int64_t stub_base; // first stub row of this sequence
+};
+
+struct SpliceParams {
+    PoolView pool;
+    const int32_t *block_tables;
+    int32_t max_blocks;
+    const char *stub_copy; // [L][total_stub][copy_dim] bf16
+    const char *stub_rot;  // [L][total_stub][rot width] bf16
+    int64_t total_stub;
+    const float4 *table; // [num_seqs][head_dim/2], row q for sequence q of this launch
+    uint32_t *status;
+    uint32_t *ticket;
+    uint32_t *flags;
+    int64_t total_tickets;
+    int64_t wait_limit_ns;
+    int32_t num_seqs;
+    SpliceSeq seq[kMaxSeqsPerLaunch];
+};
+
+struct TableParams {
+    const int32_t *d_delta;             // per-unit shifts in device memory, or ...
+    int32_t h_delta[kMaxSeqsPerLaunch]; // ... carried in the launch (d_delta == nullptr)
+    int32_t units;
+    int32_t half;     // frequencies per head
+    int32_t head_dim; // d
+    double base;
+    float4 *table;
+};
+
+} // namespace kvr

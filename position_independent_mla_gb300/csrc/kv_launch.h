@@ -1,0 +1,24 @@
+// kv_launch.h -- internal launchers (one per kernel family).
+#pragma once
+
+#include "kv_internal.h"
+
+namespace kvr {
+
+// Row shapes with a compiled kernel.
+enum class RowKind {
+    Mla, // verbatim 512 + rotary 1 x 64 (c_KV + k_pe)
+    Gqa  // verbatim 1024 + rotary 8 x 128 (V + K)
+};
+
+cudaError_t launch_delta_table(const TableParams &p, cudaStream_t stream);
+cudaError_t launch_relocate(const RelocParams &p, RowKind kind, cudaStream_t stream);
+// Launches one ticketed block per tile; `blocks` = p.total_tickets.
+cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stream);
+cudaError_t launch_wait_check(uint32_t *flag, uint32_t *status, int64_t limit_ns,
+                              cudaStream_t stream);
+
+// Rows per tile of each kind (splice workspace sizing).
+inline int tile_rows(RowKind kind) { return kind == RowKind::Mla ? kTileMla : kTileGqa; }
+
+} // namespace kvr

@@ -1,0 +1,458 @@
+"""Benchmark of the KV relocation / splice / patch path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--check]
+
+Default workload (the one the headline metric is quoted on): Irminsul-style
+relocation with a DeepSeek-V3-shaped MLA cache -- 61 layers, rows of c_KV 512
++ k_pe 64 bf16, 64-token blocks, 32 requests each assembling 16 chunks (lengths
+uniform in 256..2048 tokens) from a registry of 256 canonical chunks, δ per
+chunk uniform in [-32768, 32768].  One step = one kv_relocate call (δ-table
+kernel + relocation kernel) over the whole batch.  Other workloads:
+``splice-mla-128k`` (Leyline AMORTIZE at 128K context), ``relocate-gqa-patch``
+(Kamera GQA with a fused rank-16 patch), ``splice-mla-4k`` (one layer, 4096
+tokens).
+
+Prints one JSON line (rank 0).  ``value`` is relocated KV tokens/s over all
+layers for the whole job; ``roofline`` gives the dominant kernel's achieved
+HBM bandwidth (algorithmic bytes / CUDA-event time on its stream) against the
+measured copy peak; ``e2e`` is the same metric through the C-ABI call with the
+per-step index arrays copied from pinned host memory and the status word
+read back every step; ``cpu_baseline`` is the fp64 oracle timed on a bounded
+sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+MLA_ROW = 576           # c_KV 512 + k_pe 64 (bf16)
+MLA_ROW_BYTES = 1152
+GQA_ROW_BYTES = 4096    # K or V: 8 heads x 128 x bf16
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sources_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "position_independent_mla_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when that summary was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{workload}_traffic.txt")
+    try:
+        kv = dict(line.strip().split("=", 1) for line in open(path)
+                  if "=" in line and not line.startswith("#"))
+    except OSError:
+        return None
+    if kv.get("kernel_sources_sha256_16") != kernel_sources_hash():
+        return None
+    return float(kv["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            ident = str(torch.cuda.get_device_properties(self.device).uuid)
+            ident = ident if ident.startswith("GPU-") else "GPU-" + ident
+        except Exception:
+            ident = str(self.device)
+        self.path = f"/tmp/kvreloc_clocks_{os.getpid()}.csv"
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", ident], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def fill_normal_(t: torch.Tensor, seed: int) -> None:
+    """Fill a bf16 [L][...] device tensor with N(0,1) draws, one layer at a time."""
+    g = torch.Generator(device=t.device)
+    for l in range(t.shape[0]):
+        g.manual_seed(seed * 1000 + l)
+        t[l].copy_(torch.randn(t[l].shape, generator=g, device=t.device, dtype=torch.float32))
+
+
+# ---------------------------------------------------------------------------
+# Workload: Irminsul relocation, MLA, 61 layers (default)
+# ---------------------------------------------------------------------------
+
+RELOC_MLA = dict(layers=61, num_reqs=32, chunks_per_req=16, len_lo=256, len_hi=2048,
+                 delta_lo=-32768, delta_hi=32768, n_pool_chunks=256, base_hi=32768, base=10000.0)
+
+
+def build_relocate_mla(rank: int, device: str = "cuda", cfg=RELOC_MLA):
+    import position_independent_mla_gb300 as kv
+
+    c = cfg
+    wl = synth.relocate_workload(1002 + 100 * rank, num_reqs=c["num_reqs"],
+                                 chunks_per_req=c["chunks_per_req"], len_lo=c["len_lo"],
+                                 len_hi=c["len_hi"], delta_lo=c["delta_lo"],
+                                 delta_hi=c["delta_hi"], n_pool_chunks=c["n_pool_chunks"],
+                                 base_hi=c["base_hi"])
+    L = c["layers"]
+    src = torch.empty((L, wl.src_slots_total, MLA_ROW), dtype=torch.bfloat16, device=device)
+    fill_normal_(src, 1002 + 100 * rank)
+    dst = torch.zeros((L, wl.dst_slots_total, MLA_ROW), dtype=torch.bfloat16, device=device)
+    sd = kv.pool_desc(src[..., :512], src[..., 512:], 64, 1, c["base"])
+    dd = kv.pool_desc(dst[..., :512], dst[..., 512:], 64, 1, c["base"])
+    host = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).pin_memory()
+            for k in ("tok_off", "src_slots", "chunk_req", "chunk_dst_pos", "delta",
+                      "block_tables")}
+    dev = {k: v.to(device) for k, v in host.items()}
+    ws = kv.workspace(dd, wl.total_tokens, wl.num_chunks, device=device)
+    return dict(wl=wl, src=src, dst=dst, sd=sd, dd=dd, host=host, dev=dev, ws=ws, L=L, cfg=c)
+
+
+def relocate_call(st, dev=None, stream=None):
+    import position_independent_mla_gb300 as kv
+
+    wl, d = st["wl"], dev if dev is not None else st["dev"]
+    kv.kv_relocate(st["sd"], st["dd"], wl.num_chunks, wl.total_tokens, d["tok_off"],
+                   d["src_slots"], d["chunk_req"], d["chunk_dst_pos"], d["delta"],
+                   d["block_tables"], wl.block_tables.shape[0], wl.block_tables.shape[1], None,
+                   st["ws"], stream=stream)
+    return kv.kv_last_launch_count()
+
+
+def check_relocate_sample(st, orc, n_rows: int = 3000, seed: int = 7) -> dict:
+    """Sampled parity at full size: random (token, layer) rows of the last
+    relocation, each compared with the oracle's rotation of its source row."""
+    wl, L = st["wl"], st["L"]
+    rng = np.random.default_rng(seed)
+    toks = rng.integers(0, wl.total_tokens, n_rows)
+    lays = rng.integers(0, L, n_rows)
+    chunk = np.searchsorted(wl.tok_off, toks, side="right") - 1
+    pos = wl.chunk_dst_pos[chunk] + (toks - wl.tok_off[chunk])
+    dslot = wl.block_tables[wl.chunk_req[chunk], pos // 64].astype(np.int64) * 64 + pos % 64
+    sslot = wl.src_slots[toks].astype(np.int64)
+    li = torch.from_numpy(lays).cuda()
+    srows = st["src"][li, torch.from_numpy(sslot).cuda()].cpu()
+    drows = st["dst"][li, torch.from_numpy(dslot).cuda()].cpu()
+    sb, db = synth.bits(srows), synth.bits(drows)
+    copy_bad = int((sb[:, :512] != db[:, :512]).any(axis=1).sum())
+    exact = one = beyond = 0
+    for i in range(n_rows):
+        want = orc.rotate_bf16(sb[i, 512:], int(wl.delta[chunk[i]]), st["cfg"]["base"])
+        g = db[i, 512:].astype(np.int64)
+        w = want.astype(np.int64)
+        og = np.where(g & 0x8000, 0x8000 - (g & 0x7FFF), 0x8000 + g)
+        ow = np.where(w & 0x8000, 0x8000 - (w & 0x7FFF), 0x8000 + w)
+        dist = np.abs(og - ow)
+        exact += int((dist == 0).sum())
+        one += int((dist == 1).sum())
+        beyond += int((dist > 1).sum())
+    return {"rows": n_rows, "copy_rows_differing": copy_bad, "rot_exact": exact,
+            "rot_one_ulp": one, "rot_beyond": beyond}
+
+
+def cpu_baseline_relocate(orc, cfg=RELOC_MLA, chunks: int = 3, seed: int = 4242):
+    """Oracle relocation of a bounded sample: 1 request x `chunks` chunks drawn
+    with the workload's recipe, all layers, KV values drawn on the host."""
+    import oracle as O
+
+    c = cfg
+    wl = synth.relocate_workload(seed, num_reqs=1, chunks_per_req=chunks, len_lo=c["len_lo"],
+                                 len_hi=c["len_hi"], delta_lo=c["delta_lo"],
+                                 delta_hi=c["delta_hi"], n_pool_chunks=chunks, base_hi=63)
+    L = c["layers"]
+    src = O.Pool(synth.bits(synth.bf16_normal((L, wl.src_slots_total, 512), seed)).copy(),
+                 synth.bits(synth.bf16_normal((L, wl.src_slots_total, 64), seed + 1)).copy(),
+                 64, 1, 64, c["base"])
+    dst = O.Pool(np.zeros((L, wl.dst_slots_total, 512), np.uint16),
+                 np.zeros((L, wl.dst_slots_total, 64), np.uint16), 64, 1, 64, c["base"])
+    t0 = time.perf_counter()
+    assert orc.relocate(src, dst, wl.tok_off, wl.src_slots, wl.chunk_req, wl.chunk_dst_pos,
+                        wl.delta, wl.block_tables) == O.OK
+    dt = time.perf_counter() - t0
+    return wl.total_tokens, dt
+
+
+# A small case of the same kernel for ncu captures (a few GB on the device).
+RELOC_MLA_SMALL = dict(RELOC_MLA, num_reqs=2, n_pool_chunks=16)
+
+
+def run_relocate_mla(args, rank, world, local):
+    import position_independent_mla_gb300 as kv
+
+    st = build_relocate_mla(rank, cfg=RELOC_MLA_SMALL if args.small else RELOC_MLA)
+    wl, L = st["wl"], st["L"]
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        relocate_call(st)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    launches = 0
+    t_start.record()
+    for i in range(K):
+        kv.kv_set_kernel_events(*ev[i])
+        launches += relocate_call(st)
+    t_stop.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    kv.kv_set_kernel_events(None, None)
+    step_ms = t_start.elapsed_time(t_stop) / K
+    kern_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+
+    # end to end through the C ABI: host index arrays -> device, call, status back
+    host, dev = st["host"], st["dev"]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        relocate_call(st, dev)
+        status = kv.kv_get_device_status(st["ws"], stream)
+        assert status == kv.KV_OK, kv.status_string(status)
+    e2e_s = time.perf_counter() - t0
+    barrier(world)
+    clk = clocks.stop()
+
+    step_ms = max_over_ranks(step_ms, world)
+    kern_ms_max = max_over_ranks(kern_ms, world)
+    e2e_s = max_over_ranks(e2e_s, world)
+    tokens = wl.total_tokens
+    total_tokens = tokens * world  # weak scaling: every rank relocates its own batch
+
+    check = None
+    orc = None
+    if rank == 0 and (args.check or not args.no_cpu_baseline):
+        import oracle as O
+        orc = O.get()
+    if args.check and rank == 0:
+        check = check_relocate_sample(st, orc)
+
+    bytes_per_launch = tokens * (L * 2 * MLA_ROW_BYTES + 4)
+    peak, peak_kind = hbm_peak()
+    achieved = bytes_per_launch / (kern_ms * 1e-3) / 1e9
+    traffic = recorded_traffic("relocate_mla")
+    out = {
+        "metric": "relocated KV tokens/s (all layers)",
+        "value": total_tokens / (step_ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "impl": "ours",
+        "config": {"workload": "irminsul-relocate-mla: 61 layers, c_KV 512 + k_pe 64 bf16, "
+                               "64-token blocks, 32 requests x 16 chunks of U[256,2048] tokens "
+                               "from a 256-chunk registry, delta U[-32768,32768]",
+                   "tokens_per_step_per_gpu": tokens, "layers": L, "chunks": wl.num_chunks,
+                   "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": "inputs larger than L2 (%.1f GB moved per step)" % (
+                       bytes_per_launch / 1e9),
+                   "math": "fp64 angles, compensated fp32 rotation, one bf16 rounding"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": traffic, "kernel": "relocate_kernel<MLA>",
+                     "kernel_ms": kern_ms, "kernel_ms_max_over_ranks": kern_ms_max,
+                     "algorithmic_bytes_per_launch": bytes_per_launch},
+        "e2e": {"value": total_tokens * K / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+        "clocks": clk,
+        "gpu_launches": launches,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        ntok, dt = cpu_baseline_relocate(orc)
+        out["cpu_baseline"] = {"value": ntok / dt, "unit": "tokens/s", "cores": 1,
+                               "kind": "oracle",
+                               "sample": f"1 request x 3 chunks ({ntok} tokens) of the same "
+                                         f"recipe, all 61 layers, {dt:.1f} s single-threaded"}
+    if check is not None:
+        out["parity_sample"] = check
+    return out
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle, as it stands, on the host cores."""
+    import oracle as O
+
+    if rank != 0:
+        return None
+    orc = O.get()
+    c = RELOC_MLA
+    # calibrate, then size each step so the whole run stays within ~2 minutes
+    probe_tokens = 32
+
+    def step(n_tok, seed):
+        wl = synth.relocate_workload(seed, num_reqs=1, chunks_per_req=1, len_lo=n_tok,
+                                     len_hi=n_tok, delta_lo=c["delta_lo"], delta_hi=c["delta_hi"],
+                                     n_pool_chunks=1, base_hi=63)
+        L = c["layers"]
+        src = O.Pool(synth.bits(synth.bf16_normal((L, wl.src_slots_total, 512), seed)).copy(),
+                     synth.bits(synth.bf16_normal((L, wl.src_slots_total, 64), seed + 1)).copy(),
+                     64, 1, 64, c["base"])
+        dst = O.Pool(np.zeros((L, wl.dst_slots_total, 512), np.uint16),
+                     np.zeros((L, wl.dst_slots_total, 64), np.uint16), 64, 1, 64, c["base"])
+        t0 = time.perf_counter()
+        assert orc.relocate(src, dst, wl.tok_off, wl.src_slots, wl.chunk_req, wl.chunk_dst_pos,
+                            wl.delta, wl.block_tables) == O.OK
+        return time.perf_counter() - t0
+
+    rate = probe_tokens / step(probe_tokens, 5)
+    per_step = int(max(16, min(4096, rate * 120.0 / max(1, args.steps + args.warmup))))
+    for w in range(args.warmup):
+        step(per_step, 10 + w)
+    total = 0.0
+    for k in range(args.steps):
+        total += step(per_step, 1000 + k)
+    value = per_step * args.steps / total
+    return {
+        "metric": "relocated KV tokens/s (all layers)", "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": "irminsul-relocate-mla (bounded sample per step: 1 chunk of "
+                               f"{per_step} tokens, 61 layers)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} tokens x 61 layers per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+WORKLOADS = {"relocate-mla": run_relocate_mla}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="relocate-mla")
+    ap.add_argument("--check", action="store_true", help="sampled parity vs the oracle")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true",
+                    help="a reduced batch of the same workload (for profiler captures)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local = dist_info()
+
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+
+    import position_independent_mla_gb300 as kv
+
+    kv.load()  # raises if the CUDA library is missing: there is no fallback
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    out = WORKLOADS[args.workload](args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -198,6 +198,12 @@ void kv_set_wait_limit_ns(int64_t limit_ns);
 kv_status kv_check_wait_timeout(void *d_workspace, size_t workspace_bytes, int64_t limit_ns,
                                 kv_stream_t stream);
 
+/* Timing hook.  When both are non-NULL (cudaEvent_t handles), every later
+ * call on this thread records `start_event` on its stream just before its
+ * row-moving kernel(s) and `stop_event` just after, so the caller can time
+ * that kernel alone with cudaEventElapsedTime.  NULL, NULL turns it off. */
+void kv_set_kernel_events(void *start_event, void *stop_event);
+
 /* Number of kernels the most recent successful call on this thread enqueued. */
 int32_t kv_last_launch_count(void);
 

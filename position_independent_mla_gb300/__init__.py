@@ -89,6 +89,7 @@ def load(build_if_missing: bool = False) -> C.CDLL:
         "kv_set_wait_limit_ns": (None, [i64]),
         "kv_check_wait_timeout": (i32, [vp, sz, i64, vp]),
         "kv_last_launch_count": (i32, []),
+        "kv_set_kernel_events": (None, [vp, vp]),
         "kv_status_string": (C.c_char_p, [i32]),
         "kv_version": (i32, []),
     }
@@ -237,6 +238,13 @@ def kv_set_wait_limit_ns(limit_ns: int) -> None:
 def kv_check_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> int:
     return int(load().kv_check_wait_timeout(ws.data_ptr(), ws.numel() * ws.element_size(),
                                             int(limit_ns), _stream(stream)))
+
+
+def kv_set_kernel_events(start=None, stop=None) -> None:
+    """Record torch.cuda.Event ``start``/``stop`` around the row-moving kernel
+    of every later call on this thread (None, None = off)."""
+    load().kv_set_kernel_events(None if start is None else start.cuda_event,
+                                None if stop is None else stop.cuda_event)
 
 
 def kv_last_launch_count() -> int:

@@ -19,6 +19,12 @@ namespace {
 constexpr int64_t kDefaultWaitLimitNs = 2000000000ll;
 std::atomic<int64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 thread_local int32_t t_launches = 0;
+thread_local cudaEvent_t t_ev_start = nullptr, t_ev_stop = nullptr;
+
+cudaError_t mark(cudaEvent_t ev, cudaStream_t stream)
+{
+    return (t_ev_start && t_ev_stop) ? cudaEventRecord(ev, stream) : cudaSuccess;
+}
 
 constexpr size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
@@ -199,7 +205,9 @@ kv_status relocate_impl(const kv_pool_desc *src, const kv_pool_desc *dst, int32_
     rp.patched = patched ? 1 : 0;
     rp.in_place = in_place ? 1 : 0;
     rp.status = reinterpret_cast<uint32_t *>(w);
+    KV_CUDA(mark(t_ev_start, stream));
     KV_CUDA(launch_relocate(rp, kind, stream));
+    KV_CUDA(mark(t_ev_stop, stream));
     ++t_launches;
     return KV_OK;
 }
@@ -334,6 +342,7 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d
     uint32_t *flags = reinterpret_cast<uint32_t *>(w + kHeaderBytes + tbytes);
     KV_CUDA(cudaMemsetAsync(w, 0, kHeaderBytes, stream));
     const int64_t limit = g_wait_limit_ns.load();
+    bool marked = false;
     for (SpliceParams &sp : plans) {
         if (sp.total_tickets == 0)
             continue;
@@ -365,9 +374,15 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d
         sp.ticket = ticket;
         sp.flags = flags;
         sp.wait_limit_ns = limit;
+        if (!marked) {
+            KV_CUDA(mark(t_ev_start, stream));
+            marked = true;
+        }
         KV_CUDA(launch_splice(sp, kind, stream));
         ++t_launches;
     }
+    if (marked)
+        KV_CUDA(mark(t_ev_stop, stream));
     for (int q = 0; q < num_seqs; ++q)
         h_seq_lens[q] += h_stub_len[q] - (h_s_end[q] - h_s_start[q]);
     return KV_OK;
@@ -405,6 +420,12 @@ kv_status kv_check_wait_timeout(void *d_workspace, size_t workspace_bytes, int64
     KV_CUDA(launch_wait_check(w + 2, w, limit_ns, stream));
     ++t_launches;
     return KV_OK;
+}
+
+void kv_set_kernel_events(void *start_event, void *stop_event)
+{
+    t_ev_start = static_cast<cudaEvent_t>(start_event);
+    t_ev_stop = static_cast<cudaEvent_t>(stop_event);
 }
 
 int32_t kv_last_launch_count(void) { return t_launches; }

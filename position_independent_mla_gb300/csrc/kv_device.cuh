@@ -67,10 +67,10 @@ __device__ __forceinline__ uint32_t bf16_round(float hi, float lo)
 // The δ-table stores, per (unit, frequency j), cos(δθ_j) = c1 + c2 and
 // sin(δθ_j) = s1 + s2, formed in fp64; c1 and s1 carry at most 16
 // significant bits, so with bf16 inputs (8 bits) the products x*c1 and y*s1
-// are exact in fp32 and fmaf(x, c1, -y*s1) rounds the true difference once.
-// The c2/s2 terms add the next 24 bits.  (hi, lo) then holds the rotated
-// value to about 2^-40 of |x|+|y|, and one tie-aware rounding gives the
-// bf16 nearest to it.
+// are exact in fp32.  An error-free two-sum turns x*c1 - y*s1 into t + et
+// exactly; the small c2/s2 terms (the next 24 bits of cos and sin) are
+// added to et.  (hi, lo) then holds the rotated value to about 2^-38 of
+// |x|+|y|, and one tie-aware rounding gives the bf16 nearest to it.
 
 // Output of this lane for one pair: `first` selects x*cos - y*sin (the lane
 // holding the first half of the head) or x*sin + y*cos (second half).
@@ -81,15 +81,19 @@ __device__ __forceinline__ uint32_t rotate_one(uint32_t xb, uint32_t yb, float4 
     const float x = __uint_as_float(xb << 16), y = __uint_as_float(yb << 16);
     float hi, lo;
     if (bf16_finite(xb) && bf16_finite(yb)) {
-        float t, u;
+        float p, q, u;
         if (first) {
-            t = fmaf(x, cs.x, -(y * cs.z));
+            p = x * cs.x; // exact
+            q = -(y * cs.z); // exact
             u = fmaf(x, cs.y, -(y * cs.w));
         } else {
-            t = fmaf(x, cs.z, y * cs.x);
+            p = x * cs.z;
+            q = y * cs.x;
             u = fmaf(x, cs.w, y * cs.y);
         }
-        two_sum(t, u, hi, lo);
+        float t, et;
+        two_sum(p, q, t, et);
+        two_sum(t, et + u, hi, lo);
     } else {
         // Inf / NaN inputs: plain IEEE arithmetic, as the fp64 definition does
         const float c = cs.x + cs.y, s = cs.z + cs.w;

@@ -242,7 +242,10 @@ def kv_check_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> int:
 
 def kv_set_kernel_events(start=None, stop=None) -> None:
     """Record torch.cuda.Event ``start``/``stop`` around the row-moving kernel
-    of every later call on this thread (None, None = off)."""
+    of every later call on this thread (None, None = off).  The events must
+    have been recorded once through torch first (torch creates them lazily)."""
+    if start is not None and (start.cuda_event == 0 or stop.cuda_event == 0):
+        raise ValueError("record the events once through torch before passing them")
     load().kv_set_kernel_events(None if start is None else start.cuda_event,
                                 None if stop is None else stop.cuda_event)
 

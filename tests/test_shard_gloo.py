@@ -1,0 +1,54 @@
+"""Multi-process host logic on CPU (gloo, world size 2): the independent units
+of a batch are split across ranks with no overlap and no gap, and the
+benchmark's max-over-ranks timing reduction sees every rank.  The data path
+itself has no collective: each rank relocates its own requests."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, n_units, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    import synth
+
+    mine = list(synth.shard(n_units, rank, world))
+    got = [None] * world
+    dist.all_gather_object(got, mine)
+    t = bench.max_over_ranks(1.0 + rank, world)
+    dist.barrier()
+    if rank == 0:
+        q.put((got, t))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("n_units", [0, 1, 7, 32])
+def test_shards_cover_units_once(n_units):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, n_units, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got, t = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    flat = [u for part in got for u in part]
+    assert sorted(flat) == list(range(n_units))
+    assert abs(len(got[0]) - len(got[1])) <= 1
+    assert t == 2.0

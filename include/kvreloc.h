@@ -183,6 +183,38 @@ kv_status kv_patch(const kv_pool_desc *pool, int32_t num_chunks, int64_t total_t
                    int32_t num_reqs, int32_t max_blocks, const kv_patch_desc *patch,
                    void *d_workspace, size_t workspace_bytes, kv_stream_t stream);
 
+/* Allocation-free variant of kv_relocate.  The source pages have no
+ * counterpart of this call; it exists for callers that cannot allocate device
+ * memory: code running inside a runtime whose allocator owns all of the GPU
+ * (for example a serving engine that hands out pre-reserved HBM to its
+ * plugins and forbids further cudaMalloc), or latency-critical paths where an
+ * allocation and its implicit synchronisation are not acceptable.  Such a
+ * caller still passes the pools, index arrays and patch factors; the scratch
+ * that kv_relocate takes from its workspace (a status word and the per-chunk
+ * cos/sin table) comes instead from a fixed 2 MiB device array inside the
+ * library.  Every GPU that loads the library holds that array until the
+ * process exits.
+ *  - Limit: the table holds up to 4095 chunks for MLA rows (64-dim k_pe) and
+ *    2047 chunks for 8 x 128 GQA rows; larger num_chunks is rejected with
+ *    KV_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - All calls share the one array, which keeps the last call's contents;
+ *    each call clears its status word first.  Calls that overlap on the GPU
+ *    (different streams, not ordered) race on the array: order them.
+ *  - h_device_status: when non-NULL the call waits for `stream` and stores
+ *    the device status (KV_OK or KV_ERR_OUT_OF_RANGE) there; when NULL the
+ *    call stays asynchronous and device-side errors are not reported.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ * Arguments otherwise as kv_relocate. */
+kv_status kv_relocate_noalloc(const kv_pool_desc *src, const kv_pool_desc *dst,
+                              int32_t num_chunks, int64_t total_tokens, const int32_t *d_tok_off,
+                              const int32_t *d_src_slots, const int32_t *d_chunk_req,
+                              const int32_t *d_chunk_dst_pos, const int32_t *d_delta,
+                              const int32_t *d_block_tables, int32_t num_reqs,
+                              int32_t max_blocks, const kv_patch_desc *patch,
+                              int32_t *h_device_status, kv_stream_t stream);
+
 /* Wait for `stream`, then return the device status of the last call that
  * used this workspace (KV_OK, KV_ERR_OUT_OF_RANGE or KV_ERR_TIMEOUT), or
  * KV_ERR_CUDA if the synchronisation or the read failed. */

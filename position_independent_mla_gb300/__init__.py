@@ -90,6 +90,8 @@ def load(build_if_missing: bool = False) -> C.CDLL:
         "kv_check_wait_timeout": (i32, [vp, sz, i64, vp]),
         "kv_last_launch_count": (i32, []),
         "kv_set_kernel_events": (None, [vp, vp]),
+        "kv_relocate_noalloc": (i32, [P, P, i32, i64, vp, vp, vp, vp, vp, vp, i32, i32, PP,
+                                      C.POINTER(C.c_int32), vp]),
         "kv_status_string": (C.c_char_p, [i32]),
         "kv_version": (i32, []),
     }
@@ -256,3 +258,22 @@ def kv_last_launch_count() -> int:
 
 def kv_version() -> int:
     return int(load().kv_version())
+
+
+def kv_relocate_noalloc(src: kv_pool_desc, dst: kv_pool_desc, num_chunks: int,
+                        total_tokens: int, tok_off, src_slots, chunk_req, chunk_dst_pos, delta,
+                        block_tables, num_reqs: int, max_blocks: int,
+                        patch: Optional[kv_patch_desc], stream=None, wait: bool = True,
+                        check: bool = True):
+    """kv_relocate for callers that cannot allocate device memory: no workspace
+    argument; the library's built-in device scratch is used instead.  With
+    ``wait`` the call synchronises and returns (status, device_status)."""
+    dev_status = C.c_int32(-1)
+    st = load().kv_relocate_noalloc(
+        C.byref(src), C.byref(dst), int(num_chunks), int(total_tokens), _ptr(tok_off),
+        _ptr(src_slots), _ptr(chunk_req), _ptr(chunk_dst_pos), _ptr(delta), _ptr(block_tables),
+        int(num_reqs), int(max_blocks), C.byref(patch) if patch is not None else None,
+        C.byref(dev_status) if wait else None, _stream(stream))
+    if check:
+        _check(st, "kv_relocate_noalloc")
+    return st, (int(dev_status.value) if wait else None)

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "kvreloc.h"
@@ -456,3 +457,73 @@ const char *kv_status_string(kv_status s)
 int32_t kv_version(void) { return 100; }
 
 } // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free relocation
+// ---------------------------------------------------------------------------
+//
+// kv_relocate needs a little device scratch (a status word and the per-chunk
+// cos/sin table).  Callers that cannot allocate device memory themselves get
+// it from this fixed array instead of a workspace argument.  The array is a
+// device global: every GPU that loads the library keeps these bytes until
+// the process exits.  Host code may not use its name as an address (on the
+// host it only names a stand-in object), so its device address is fetched
+// once per device with cudaGetSymbolAddress and passed to the kernels.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20; // 2 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device (set up on the
+// first call made with that device current).
+kv_status noalloc_scratch(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+        return KV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return KV_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return KV_OK;
+}
+
+} // namespace
+
+extern "C" kv_status kv_relocate_noalloc(const kv_pool_desc *src, const kv_pool_desc *dst,
+                                         int32_t num_chunks, int64_t total_tokens,
+                                         const int32_t *d_tok_off, const int32_t *d_src_slots,
+                                         const int32_t *d_chunk_req,
+                                         const int32_t *d_chunk_dst_pos, const int32_t *d_delta,
+                                         const int32_t *d_block_tables, int32_t num_reqs,
+                                         int32_t max_blocks, const kv_patch_desc *patch,
+                                         int32_t *h_device_status, kv_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    void *scratch = nullptr;
+    kv_status st = noalloc_scratch(&scratch);
+    if (st != KV_OK)
+        return st;
+    // the shared relocation path; it clears the status word before launching
+    st = relocate_impl(src, dst, num_chunks, total_tokens, d_tok_off, d_src_slots, d_chunk_req,
+                       d_chunk_dst_pos, d_delta, d_block_tables, num_reqs, max_blocks, patch,
+                       scratch, kNoAllocScratchBytes, stream, false);
+    if (st != KV_OK || h_device_status == nullptr)
+        return st;
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, scratch, sizeof word, cudaMemcpyDeviceToHost, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return KV_ERR_CUDA;
+    *h_device_status = static_cast<int32_t>(word);
+    return KV_OK;
+}

@@ -323,7 +323,7 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d
             S.flag_base = flags;
             S.stub_base = stub_base;
             tickets += S.n_shift + S.n_stub;
-            flags += (int64_t)S.n_shift * L;
+            flags += S.n_shift;
             stub_base += S.n_r;
         }
         sp.total_tickets = tickets;
@@ -349,7 +349,7 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d
             continue;
         int64_t nflags = 0;
         for (int i = 0; i < sp.num_seqs; ++i)
-            nflags += (int64_t)sp.seq[i].n_shift * L;
+            nflags += sp.seq[i].n_shift;
         KV_CUDA(cudaMemsetAsync(ticket, 0, sizeof(uint32_t), stream));
         if (nflags > 0)
             KV_CUDA(cudaMemsetAsync(flags, 0, (size_t)nflags * 4u, stream));

@@ -204,6 +204,28 @@ static __device__ __noinline__ bool wait_flag(const uint32_t *flag, int64_t limi
     return ld_acquire(flag) != 0u;
 }
 
+// Spin until *counter >= want, bounded as wait_flag; returns the last value
+// read (>= want on success).
+static __device__ __noinline__ uint32_t wait_count(const uint32_t *counter, uint32_t want,
+                                                   int64_t limit_ns)
+{
+    const uint64_t t0 = global_ns();
+    const uint64_t max_polls = (uint64_t)limit_ns / 16u + 4096u;
+    unsigned sleep_ns = 32;
+    uint32_t v = 0;
+    for (uint64_t it = 0; it < max_polls; ++it) {
+        v = ld_acquire(counter);
+        if (v >= want)
+            return v;
+        if ((int64_t)(global_ns() - t0) > limit_ns)
+            return v;
+        __nanosleep(sleep_ns);
+        if (sleep_ns < 2048)
+            sleep_ns <<= 1;
+    }
+    return ld_acquire(counter);
+}
+
 // Physical slot of logical position pos in a block-table row, or -1 when
 // the position or the block id falls outside the table or the pool.
 __device__ __forceinline__ int64_t slot_of(const int32_t *bt_row, int32_t max_blocks,

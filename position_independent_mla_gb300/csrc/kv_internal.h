@@ -65,7 +65,7 @@ struct SpliceSeq {
     int32_t n_stub;  // stub tiles
     int32_t bt_row;  // block-table row
     int64_t ticket_base;
-    int64_t flag_base; // flags of this sequence: [n_shift][L]
+    int64_t flag_base; // per-tile "layers read" counters of this sequence: [n_shift]
     int64_t stub_base; // first stub row of this sequence
 };
 

@@ -51,7 +51,7 @@ cudaError_t launch_delta_table(const TableParams &p, cudaStream_t stream)
 // ---------------------------------------------------------------------------
 
 template <class G, bool PATCH>
-__global__ void __launch_bounds__(kThreads) relocate_kernel(const __grid_constant__ RelocParams p)
+__global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const __grid_constant__ RelocParams p)
 {
     __shared__ int64_t s_src[G::T];
     __shared__ int64_t s_dst[G::T];

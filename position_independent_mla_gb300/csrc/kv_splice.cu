@@ -12,23 +12,28 @@
 // tiles come last.  A tile's destination range overlaps the source range of
 // at most two earlier tiles.  Each block takes a ticket from an atomic
 // counter (so tickets are handed out in launch order, and every tile a block
-// waits for belongs to a block that is already running), and then, layer by
-// layer: loads its rows, publishes "rows of this layer read" with a release
-// store, waits (acquire, bounded) for the same flag of the tiles it
-// overwrites, and stores.  The earliest unfinished tile never waits on an
-// unfinished one, so the protocol cannot deadlock; the bound on each wait
-// turns any unforeseen stall into KV_ERR_TIMEOUT instead of a hang.
+// waits for belongs to a block that is already running).  Every shift tile
+// owns a counter: the number of layers whose rows it has read, published
+// with a release store.  Layer by layer a block loads its rows; thread 0
+// makes sure (acquire, bounded) that the tiles it overwrites have read this
+// layer -- a value seen once covers all layers up to it, so a dependency far
+// behind costs one poll for the whole tile -- then one barrier, the block's
+// own counter is published, and the rows are stored.  The earliest
+// unfinished tile never waits on an unfinished one, so the protocol cannot
+// deadlock; the bound on each wait turns any unforeseen stall into
+// KV_ERR_TIMEOUT instead of a hang.
 #include "kv_launch.h"
 #include "kv_tiles.cuh"
 
 namespace kvr {
 
 template <class G>
-__global__ void __launch_bounds__(kThreads) splice_kernel(const __grid_constant__ SpliceParams p)
+__global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const __grid_constant__ SpliceParams p)
 {
     __shared__ uint32_t s_ticket;
-    __shared__ int32_t s_abort;
+    __shared__ volatile int32_t s_abort; // 0 -> 1 once a wait ran out; never reset
     __shared__ int64_t s_dep[2];
+    __shared__ uint32_t s_seen[2];
     __shared__ int64_t s_src[G::T];
     __shared__ int64_t s_dst[G::T];
     __shared__ int32_t s_ident[G::T];
@@ -94,6 +99,7 @@ __global__ void __launch_bounds__(kThreads) splice_kernel(const __grid_constant_
     if (tid == 0) {
         // earlier tiles whose source rows this tile's destination overlaps
         s_dep[0] = s_dep[1] = -1;
+        s_seen[0] = s_seen[1] = 0u;
         const int64_t dlo = shift ? lo + S.delta : (int64_t)S.s_start + lo;
         const int64_t dhi = shift ? hi + S.delta : (int64_t)S.s_start + hi;
         const int64_t a = max(dlo, (int64_t)S.s_end), b = min(dhi, (int64_t)S.seq_len);
@@ -135,25 +141,24 @@ __global__ void __launch_bounds__(kThreads) splice_kernel(const __grid_constant_
         const uint32_t f = fold_tile<G>(regs);
         if (p.total_tickets < 0)
             s_sink = f;
-        __syncthreads();
-        if (tid == 0) {
-            if (shift) {
-                __threadfence();
-                st_release(p.flags + S.flag_base + k * L + l, 1u);
-            }
-            if (!s_abort) {
-                for (int d = 0; d < 2; ++d) {
-                    if (s_dep[d] < 0)
-                        continue;
-                    if (!wait_flag(p.flags + S.flag_base + s_dep[d] * L + l, p.wait_limit_ns)) {
-                        set_status(p.status, kStatusTimeout);
-                        s_abort = 1;
-                        break;
-                    }
+        if (tid == 0 && !s_abort) {
+            // the tiles this one overwrites must have read layer l
+            for (int d = 0; d < 2; ++d) {
+                if (s_dep[d] < 0 || s_seen[d] > (uint32_t)l)
+                    continue;
+                const uint32_t seen = wait_count(p.flags + S.flag_base + s_dep[d], (uint32_t)l + 1u,
+                                                 p.wait_limit_ns);
+                if (seen <= (uint32_t)l) {
+                    set_status(p.status, kStatusTimeout);
+                    s_abort = 1;
+                    break;
                 }
+                s_seen[d] = seen;
             }
         }
         __syncthreads();
+        if (tid == 0 && shift)
+            st_release(p.flags + S.flag_base + k, (uint32_t)l + 1u); // layer l read
         if (!s_abort)
             store_tile<G, false>(pool_l, s_dst, regs, s_cs, 0, s_ident, none);
     }

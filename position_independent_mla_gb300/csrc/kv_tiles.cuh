@@ -14,9 +14,10 @@
 
 namespace kvr {
 
-template <int T_, int CV_, int NH_, int HV_>
+template <int T_, int CV_, int NH_, int HV_, int MIN_BLOCKS_>
 struct Geo {
     static constexpr int T = T_;
+    static constexpr int kMinBlocks = MIN_BLOCKS_; // resident blocks per SM to aim for
     static constexpr int CV = CV_;          // verbatim vectors per row
     static constexpr int NH = NH_;          // rotary heads
     static constexpr int HV = HV_;          // vectors per half head
@@ -31,9 +32,9 @@ struct Geo {
 };
 
 // MLA rows: c_KV 512 + k_pe 64 (DeepSeek-V2/V3 shape).
-using GeoMla = Geo<kTileMla, 64, 1, 4>;
+using GeoMla = Geo<kTileMla, 64, 1, 4, 4>;
 // GQA rows: V 8x128 + K 8x128 (Llama-3-8B shape).
-using GeoGqa = Geo<kTileGqa, 128, 8, 8>;
+using GeoGqa = Geo<kTileGqa, 128, 8, 8, 2>;
 
 // Where the rows of a tile live for one layer: row r's verbatim part starts
 // at cbase + idx[r]*cstride, its rotary part at rbase + idx[r]*rstride

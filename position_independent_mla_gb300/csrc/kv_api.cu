@@ -207,7 +207,10 @@ kv_status relocate_impl(const kv_pool_desc *src, const kv_pool_desc *dst, int32_
     rp.in_place = in_place ? 1 : 0;
     rp.status = reinterpret_cast<uint32_t *>(w);
     KV_CUDA(mark(t_ev_start, stream));
-    KV_CUDA(launch_relocate(rp, kind, stream));
+    if (patch_chunk_supported(rp))
+        KV_CUDA(launch_patch_chunks(rp, kind, stream));
+    else
+        KV_CUDA(launch_relocate(rp, kind, stream));
     KV_CUDA(mark(t_ev_stop, stream));
     ++t_launches;
     return KV_OK;

@@ -121,6 +121,19 @@ def test_relocate_with_fused_patch(orc, shape):
     check_pool(dst, f"relocate+patch {shape}", copy_exact=False)
 
 
+@pytest.mark.parametrize("m", [32, 64])
+def test_relocate_with_fused_patch_large_rank(orc, m):
+    # ranks above 16 take the general per-item path
+    wl, src, dst, dev = _reloc_case("gqa", 235, num_reqs=2, chunks=3, deltas=[0, 99])
+    us = [synth.f32_normal((L, wl.total_tokens, m), 236 + i, std=0.01) for i in range(2)]
+    vs = [synth.f32_normal((L, wl.num_chunks, 1024, m), 238 + i, std=0.01) for i in range(2)]
+    pd = kv.patch_desc(m, [x.cuda() for x in us], [x.cuda() for x in vs])
+    assert _run_relocate(wl, src, dst, dev, patch=pd) == kv.KV_OK
+    _oracle_relocate(orc, wl, src, dst,
+                     O.Patch(m, [x.numpy() for x in us], [x.numpy() for x in vs]))
+    check_pool(dst, f"relocate+patch rank {m}", copy_exact=False)
+
+
 @pytest.mark.parametrize("shape", ["mla", "gqa"])
 def test_standalone_patch(orc, shape):
     wl, src, dst, dev = _reloc_case(shape, 240)

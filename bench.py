@@ -42,7 +42,7 @@ import synth  # noqa: E402
 
 MLA_ROW = 576           # c_KV 512 + k_pe 64 (bf16)
 MLA_ROW_BYTES = 1152
-GQA_ROW_BYTES = 4096    # K or V: 8 heads x 128 x bf16
+GQA_ROW_BYTES = 2048    # K or V: 8 heads x 128 x bf16
 FALLBACK_HBM_GBS = 6800.0
 
 

@@ -142,9 +142,11 @@ def pool_desc(copy: torch.Tensor, rot: torch.Tensor, block_size: int, rot_heads:
     assert copy.dim() == 3 and rot.dim() == 3 and copy.stride(2) == 1 and rot.stride(2) == 1
     assert copy.shape[:2] == rot.shape[:2]
     L, S, cd = copy.shape
-    return kv_pool_desc(L, block_size, S, copy.data_ptr(), copy.stride(0), copy.stride(1), cd,
-                        rot.data_ptr(), rot.stride(0), rot.stride(1), rot_heads,
-                        rot.shape[2] // rot_heads, float(rope_base))
+    d = kv_pool_desc(L, block_size, S, copy.data_ptr(), copy.stride(0), copy.stride(1), cd,
+                     rot.data_ptr(), rot.stride(0), rot.stride(1), rot_heads,
+                     rot.shape[2] // rot_heads, float(rope_base))
+    d._tensors = (copy, rot)  # the descriptor keeps the memory it points at alive
+    return d
 
 
 def patch_desc(rank: int, u: Sequence[Optional[torch.Tensor]],
@@ -154,6 +156,7 @@ def patch_desc(rank: int, u: Sequence[Optional[torch.Tensor]],
     strides with a unit last stride; None = channel not patched."""
     d = kv_patch_desc()
     d.rank = rank
+    d._tensors = (list(u), list(v))  # keep the factors alive as long as the descriptor
     for ch in range(2):
         if u[ch] is None or v[ch] is None:
             continue

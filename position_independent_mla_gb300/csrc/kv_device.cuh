@@ -105,6 +105,42 @@ __device__ __forceinline__ uint32_t rotate_one(uint32_t xb, uint32_t yb, float4 
     return bf16_round(s, e);
 }
 
+// Patched values are held to 1 bf16 ulp (the fp32 patch sum carries its
+// own ~1e-10 error), so they take a shorter path than the exact rotation.
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// fp32 -> bf16, round to nearest even; NaN -> 0x7FC0.
+__device__ __forceinline__ uint32_t bf16_rne(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    const uint32_t r = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+    return ((u & 0x7FFFFFFFu) > 0x7F800000u) ? 0x7FC0u : r;
+}
+
+// rnd(R(δ)·(x, y) + add) for this lane's half, with two FMAs per product
+// (cos = c1 + c2, sin = s1 + s2 from the table).
+__device__ __forceinline__ uint32_t rotate_add_fast(uint32_t xb, uint32_t yb, float4 cs,
+                                                    bool first, float add)
+{
+    const float x = __uint_as_float(xb << 16), y = __uint_as_float(yb << 16);
+    if (!(bf16_finite(xb) && bf16_finite(yb))) {
+        // Inf / NaN inputs: plain IEEE arithmetic, as the fp64 definition does
+        const float c = cs.x + cs.y, s = cs.z + cs.w;
+        return bf16_rne((first ? (x * c - y * s) : (x * s + y * c)) + add);
+    }
+    float t, u;
+    if (first) {
+        t = fmaf(x, cs.x, -(y * cs.z));
+        u = fmaf(x, cs.y, -(y * cs.w));
+    } else {
+        t = fmaf(x, cs.z, y * cs.x);
+        u = fmaf(x, cs.w, y * cs.y);
+    }
+    return bf16_rne(t + (u + add));
+}
+
 // x + add, rounded once (patch on a verbatim value).
 __device__ __forceinline__ uint32_t add_round(uint32_t xb, float add)
 {

@@ -18,27 +18,32 @@
 namespace kvr {
 
 // COPY: verbatim columns; NH x D: rotary heads; CPT: columns per thread;
-// G: rows per stage; NS: stages in the ring.
-template <int COPY_, int NH_, int D_, int CPT_, int G_, int NS_, int MIN_BLOCKS_>
+// G: rows per stage; NS: stages in the ring.  SPLIT: one block per channel
+// (verbatim part or rotary part, which must then have the same width)
+// instead of one block covering the whole row.
+template <int COPY_, int NH_, int D_, int CPT_, int G_, int NS_, int MIN_BLOCKS_, bool SPLIT_>
 struct PatchGeo {
     static constexpr int COPY = COPY_, NH = NH_, D = D_, CPT = CPT_, G = G_, NS = NS_;
     static constexpr int kMinBlocks = MIN_BLOCKS_;
+    static constexpr bool SPLIT = SPLIT_;
     static constexpr int ROT = NH * D;
-    static constexpr int COLS = COPY + ROT;
-    static constexpr int NT = COLS / CPT;               // threads per block
-    static constexpr int ROW_BYTES = COLS * 2;
-    static constexpr int VEC_PER_ROW = ROW_BYTES / 16;  // 16-byte copies per row
-    static constexpr int COPY_VECS = COPY * 2 / 16;
+    static constexpr int COLS = SPLIT ? COPY : COPY + ROT; // columns a block covers
+    static constexpr int NT = COLS / CPT;                 // threads per block
+    static constexpr int ROW_BYTES = COLS * 2;            // bytes of a row a block stages
+    static constexpr int VEC_PER_ROW = ROW_BYTES / 16;    // 16-byte copies per row
+    static constexpr int COPY_VECS = SPLIT ? VEC_PER_ROW : COPY * 2 / 16;
     static constexpr int STAGE_VECS = G * VEC_PER_ROW;
-    static constexpr int MMAX = 16;                     // largest rank this kernel takes
+    static constexpr int NCH = SPLIT ? 1 : 2;             // channels a block stages U for
+    static constexpr int MMAX = 16;                       // largest rank this kernel takes
     static constexpr int HALF = D / 2;
     static_assert(NT % 32 == 0, "whole warps");
-    static_assert(COPY % (32 * CPT) == 0, "warps do not straddle the two parts");
+    static_assert(SPLIT ? COPY == ROT : COPY % (32 * CPT) == 0, "channel layout");
     static_assert(CPT % 2 == 0, "columns come in fp32 pairs");
+    static_assert(G % 2 == 0, "rows are processed in pairs");
 };
 
-using PatchGeoMla = PatchGeo<512, 1, 64, 2, 8, 4, 2>;   // 288 threads
-using PatchGeoGqa = PatchGeo<1024, 8, 128, 4, 4, 4, 1>; // 512 threads
+using PatchGeoMla = PatchGeo<512, 1, 64, 2, 8, 4, 2, false>;  // 288 threads, c_KV + k_pe
+using PatchGeoGqa = PatchGeo<1024, 8, 128, 4, 8, 4, 2, true>; // 256 threads per channel
 
 __device__ __forceinline__ void cp_async16(uint32_t smem, const void *gmem)
 {
@@ -56,15 +61,28 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// acc(2) += u * v(2), one packed fp32x2 FMA.
-__device__ __forceinline__ float2 ffma2(float u, float2 v, float2 acc)
+// Two fp32 values in one 64-bit register pair (the operand form of the
+// packed fp32x2 instructions).
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pack2(float a, float b)
 {
-    unsigned long long a, b, c;
-    a = (unsigned long long)__float_as_uint(u) | ((unsigned long long)__float_as_uint(u) << 32);
-    b = (unsigned long long)__float_as_uint(v.x) | ((unsigned long long)__float_as_uint(v.y) << 32);
-    c = (unsigned long long)__float_as_uint(acc.x) | ((unsigned long long)__float_as_uint(acc.y) << 32);
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(c) : "l"(a), "l"(b));
-    return make_float2(__uint_as_float((uint32_t)c), __uint_as_float((uint32_t)(c >> 32)));
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ float2 unpack2(f32x2 r)
+{
+    float a, b;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+    return make_float2(a, b);
+}
+
+// acc += uu * v on both halves: one fma.rn.f32x2.
+__device__ __forceinline__ void ffma2(f32x2 &acc, f32x2 uu, f32x2 v)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(uu), "l"(v));
 }
 
 template <class P, bool RELOC>
@@ -72,15 +90,15 @@ __global__ void __launch_bounds__(P::NT, P::kMinBlocks)
 patch_chunk_kernel(const __grid_constant__ RelocParams p)
 {
     extern __shared__ __align__(16) unsigned char smem[];
-    unsigned char *ring = smem;                                        // [NS][G][ROW_BYTES]
-    float *u_s = reinterpret_cast<float *>(smem + P::NS * P::G * P::ROW_BYTES); // [NS][2][G][MMAX]
+    unsigned char *ring = smem; // [NS][G][ROW_BYTES]
+    float *u_s = reinterpret_cast<float *>(smem + P::NS * P::G * P::ROW_BYTES); // [NS][NCH][G][MMAX]
     __shared__ int64_t s_src[P::NS + 1][P::G];
     __shared__ int64_t s_dst[P::NS + 1][P::G];
 
     const int tid = threadIdx.x;
     const int c = blockIdx.x;
     const int l = blockIdx.y;
-    if (c == 0 && l == 0 && tid == 0) {
+    if (c == 0 && l == 0 && blockIdx.z == 0 && tid == 0) {
         if (p.tok_off[0] != 0 || p.tok_off[p.num_chunks] != p.total_tokens)
             set_status(p.status, kStatusOutOfRange);
     }
@@ -94,38 +112,38 @@ patch_chunk_kernel(const __grid_constant__ RelocParams p)
     const int m = p.patch.m;
     const int64_t nstages = (n + P::G - 1) / P::G;
 
-    // this thread's columns
+    // this thread's channel and columns
     const int col = tid * P::CPT;
-    const int ch = col < P::COPY ? 0 : 1;
-    const int cc = ch == 0 ? col : col - P::COPY;
+    const int ch = P::SPLIT ? (int)blockIdx.z : (col < P::COPY ? 0 : 1);
+    const int cc = (P::SPLIT || ch == 0) ? col : col - P::COPY;
+    const int ch0 = P::SPLIT ? ch : 0;           // first channel staged by this block
     const bool patched = p.patch.u[ch] != nullptr;
     const int j0 = cc % P::D;
     const bool first = j0 < P::HALF;
     const int partner = ch == 1 ? (first ? cc + P::HALF : cc - P::HALF) : 0;
+    // byte offset of channel ch inside a staged row
+    const int ch_off = (P::SPLIT || ch == 0) ? 0 : P::COPY * 2;
 
-    // V factors of my columns (registers, whole chunk), as fp32 pairs
-    float2 v2[P::CPT / 2][P::MMAX];
+    // V factors of my columns (registers, whole chunk), as rank pairs:
+    // v2[e][q] = (V(col_e, 2q), V(col_e, 2q+1))
+    f32x2 v2[P::CPT][P::MMAX / 2];
 #pragma unroll
-    for (int e = 0; e < P::CPT / 2; ++e)
+    for (int e = 0; e < P::CPT; ++e)
 #pragma unroll
-        for (int r = 0; r < P::MMAX; ++r)
-            v2[e][r] = make_float2(0.f, 0.f);
+        for (int q = 0; q < P::MMAX / 2; ++q)
+            v2[e][q] = 0ull;
     if (patched) {
         const float *vb = p.patch.v[ch] + (int64_t)l * p.patch.v_ls[ch] +
                           (int64_t)c * p.patch.v_cs[ch];
 #pragma unroll
-        for (int e = 0; e < P::CPT / 2; ++e) {
-            const float *va = vb + (int64_t)(cc + 2 * e) * p.patch.v_cols[ch];
-            const float *vbb = va + p.patch.v_cols[ch];
+        for (int e = 0; e < P::CPT; ++e) {
+            const float *va = vb + (int64_t)(cc + e) * p.patch.v_cols[ch];
 #pragma unroll
             for (int r = 0; r < P::MMAX; r += 4) {
                 if (r < m) {
                     const float4 a = __ldg(reinterpret_cast<const float4 *>(va + r));
-                    const float4 b = __ldg(reinterpret_cast<const float4 *>(vbb + r));
-                    v2[e][r] = make_float2(a.x, b.x);
-                    v2[e][r + 1] = make_float2(a.y, b.y);
-                    v2[e][r + 2] = make_float2(a.z, b.z);
-                    v2[e][r + 3] = make_float2(a.w, b.w);
+                    v2[e][r / 2] = pack2(a.x, a.y);
+                    v2[e][r / 2 + 1] = pack2(a.z, a.w);
                 }
             }
         }
@@ -175,20 +193,23 @@ patch_chunk_kernel(const __grid_constant__ RelocParams p)
                 const int64_t sl = s_src[slot][row];
                 if (sl < 0)
                     continue;
-                const char *g = v < P::COPY_VECS ? src_copy + sl * sp.copy_ss + v * 16
-                                                 : src_rot + sl * sp.rot_ss + (v - P::COPY_VECS) * 16;
+                const bool in_copy = P::SPLIT ? ch == 0 : v < P::COPY_VECS;
+                const int vo = P::SPLIT ? v : (in_copy ? v : v - P::COPY_VECS);
+                const char *g = in_copy ? src_copy + sl * sp.copy_ss + vo * 16
+                                        : src_rot + sl * sp.rot_ss + vo * 16;
                 cp_async16(ring_base + (uint32_t)((buf * P::G + row) * P::ROW_BYTES + v * 16), g);
             }
-            // U rows: [2][G][m] floats, 4 per copy
+            // U rows: [NCH][G][m] floats, 4 per copy
             const int uv = m / 4;
-            for (int q = tid; q < 2 * P::G * uv; q += P::NT) {
-                const int cch = q / (P::G * uv), row = (q / uv) % P::G, r4 = q % uv;
+            for (int q = tid; q < P::NCH * P::G * uv; q += P::NT) {
+                const int k = q / (P::G * uv), row = (q / uv) % P::G, r4 = q % uv;
+                const int cch = ch0 + k;
                 const int64_t i = s * P::G + row;
                 if (p.patch.u[cch] == nullptr || i >= n)
                     continue;
                 const float *g = p.patch.u[cch] + (int64_t)l * p.patch.u_ls[cch] +
                                  (t0 + i) * p.patch.u_ts[cch] + r4 * 4;
-                cp_async16(u_base + (uint32_t)((((buf * 2 + cch) * P::G + row) * P::MMAX + r4 * 4) * 4), g);
+                cp_async16(u_base + (uint32_t)((((buf * P::NCH + k) * P::G + row) * P::MMAX + r4 * 4) * 4), g);
             }
         }
         cp_async_commit();
@@ -200,8 +221,9 @@ patch_chunk_kernel(const __grid_constant__ RelocParams p)
     for (int s = 0; s < P::NS - 1; ++s)
         issue(s);
 
-    char *dst_copy = p.dst.copy + (int64_t)l * p.dst.copy_ls;
-    char *dst_rot = p.dst.rot + (int64_t)l * p.dst.rot_ls;
+    char *dst_base = ch == 0 ? p.dst.copy + (int64_t)l * p.dst.copy_ls
+                             : p.dst.rot + (int64_t)l * p.dst.rot_ls;
+    const int64_t dst_ss = ch == 0 ? p.dst.copy_ss : p.dst.rot_ss;
     for (int64_t s = 0; s < nstages; ++s) {
         cp_async_wait<P::NS - 2>();
         __syncthreads();
@@ -209,77 +231,97 @@ patch_chunk_kernel(const __grid_constant__ RelocParams p)
         plan(s + P::NS);
         const int slot = (int)(s % (P::NS + 1));
         const int buf = (int)(s % P::NS);
+        // two rows per step: independent FMA and rounding chains interleave
 #pragma unroll 1
-        for (int row = 0; row < P::G; ++row) {
-            const int64_t d = s_dst[slot][row];
-            if (d < 0)
-                continue;
-            const unsigned char *rb = ring + (buf * P::G + row) * P::ROW_BYTES;
-            // patch term of my columns
-            float2 acc[P::CPT / 2];
+        for (int row0 = 0; row0 < P::G; row0 += 2) {
+            int64_t d[2];
+            float add[2][P::CPT];
+            const unsigned char *rb[2];
 #pragma unroll
-            for (int e = 0; e < P::CPT / 2; ++e)
-                acc[e] = make_float2(0.f, 0.f);
+            for (int k = 0; k < 2; ++k) {
+                d[k] = s_dst[slot][row0 + k];
+                rb[k] = ring + (buf * P::G + row0 + k) * P::ROW_BYTES;
+            }
             if (patched) {
-                const float4 *ur =
-                    reinterpret_cast<const float4 *>(u_s + ((buf * 2 + ch) * P::G + row) * P::MMAX);
+                f32x2 acc[2][P::CPT];
 #pragma unroll
-                for (int r = 0; r < P::MMAX; r += 4) {
-                    if (r < m) {
-                        const float4 u = ur[r / 4];
+                for (int k = 0; k < 2; ++k)
 #pragma unroll
-                        for (int e = 0; e < P::CPT / 2; ++e) {
-                            acc[e] = ffma2(u.x, v2[e][r], acc[e]);
-                            acc[e] = ffma2(u.y, v2[e][r + 1], acc[e]);
-                            acc[e] = ffma2(u.z, v2[e][r + 2], acc[e]);
-                            acc[e] = ffma2(u.w, v2[e][r + 3], acc[e]);
+                    for (int e = 0; e < P::CPT; ++e)
+                        acc[k][e] = 0ull;
+                const f32x2 *ur0 = reinterpret_cast<const f32x2 *>(
+                    u_s + ((buf * P::NCH + (ch - ch0)) * P::G + row0) * P::MMAX);
+                const f32x2 *ur1 = ur0 + P::MMAX / 2;
+#pragma unroll
+                for (int q = 0; q < P::MMAX / 2; ++q) {
+                    if (2 * q < m) {
+                        const f32x2 u0 = ur0[q], u1 = ur1[q];
+#pragma unroll
+                        for (int e = 0; e < P::CPT; ++e) {
+                            ffma2(acc[0][e], u0, v2[e][q]);
+                            ffma2(acc[1][e], u1, v2[e][q]);
                         }
                     }
                 }
-            }
-            float add[P::CPT];
 #pragma unroll
-            for (int e = 0; e < P::CPT / 2; ++e) {
-                add[2 * e] = acc[e].x;
-                add[2 * e + 1] = acc[e].y;
-            }
-            // my values (and the partner half for a rotation)
-            const unsigned char *xp = rb + (ch == 0 ? cc * 2 : P::COPY * 2 + cc * 2);
-            uint32_t xw[P::CPT / 2], yw[P::CPT / 2];
+                for (int k = 0; k < 2; ++k)
 #pragma unroll
-            for (int e = 0; e < P::CPT / 2; ++e)
-                xw[e] = reinterpret_cast<const uint32_t *>(xp)[e];
-            uint32_t out[P::CPT / 2];
-            if (ch == 1 && !ident) {
-                const unsigned char *yp = rb + P::COPY * 2 + partner * 2;
-#pragma unroll
-                for (int e = 0; e < P::CPT / 2; ++e)
-                    yw[e] = reinterpret_cast<const uint32_t *>(yp)[e];
-#pragma unroll
-                for (int e = 0; e < P::CPT / 2; ++e) {
-                    const uint32_t x0 = first ? (xw[e] & 0xFFFFu) : (yw[e] & 0xFFFFu);
-                    const uint32_t y0 = first ? (yw[e] & 0xFFFFu) : (xw[e] & 0xFFFFu);
-                    const uint32_t x1 = first ? (xw[e] >> 16) : (yw[e] >> 16);
-                    const uint32_t y1 = first ? (yw[e] >> 16) : (xw[e] >> 16);
-                    out[e] = rotate_one(x0, y0, cs[2 * e], first, add[2 * e]) |
-                             (rotate_one(x1, y1, cs[2 * e + 1], first, add[2 * e + 1]) << 16);
-                }
-            } else if (patched) {
-#pragma unroll
-                for (int e = 0; e < P::CPT / 2; ++e)
-                    out[e] = add_round(xw[e] & 0xFFFFu, add[2 * e]) |
-                             (add_round(xw[e] >> 16, add[2 * e + 1]) << 16);
+                    for (int e = 0; e < P::CPT; ++e) {
+                        const float2 a = unpack2(acc[k][e]);
+                        add[k][e] = a.x + a.y;
+                    }
             } else {
 #pragma unroll
-                for (int e = 0; e < P::CPT / 2; ++e)
-                    out[e] = xw[e];
+                for (int k = 0; k < 2; ++k)
+#pragma unroll
+                    for (int e = 0; e < P::CPT; ++e)
+                        add[k][e] = 0.0f;
             }
-            char *dp = ch == 0 ? dst_copy + d * p.dst.copy_ss + cc * 2
-                               : dst_rot + d * p.dst.rot_ss + cc * 2;
-            if (P::CPT == 4)
-                __stcs(reinterpret_cast<uint2 *>(dp), make_uint2(out[0], out[P::CPT / 2 - 1]));
-            else
-                __stcs(reinterpret_cast<unsigned int *>(dp), out[0]);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                if (d[k] < 0)
+                    continue;
+                // my values (and the partner half for a rotation)
+                const unsigned char *xp = rb[k] + ch_off + cc * 2;
+                uint32_t xw[P::CPT / 2], yw[P::CPT / 2], out[P::CPT / 2];
+#pragma unroll
+                for (int e = 0; e < P::CPT / 2; ++e)
+                    xw[e] = reinterpret_cast<const uint32_t *>(xp)[e];
+                if (ch == 1 && !ident) {
+                    const unsigned char *yp = rb[k] + ch_off + partner * 2;
+#pragma unroll
+                    for (int e = 0; e < P::CPT / 2; ++e)
+                        yw[e] = reinterpret_cast<const uint32_t *>(yp)[e];
+#pragma unroll
+                    for (int e = 0; e < P::CPT / 2; ++e) {
+                        const uint32_t x0 = first ? (xw[e] & 0xFFFFu) : (yw[e] & 0xFFFFu);
+                        const uint32_t y0 = first ? (yw[e] & 0xFFFFu) : (xw[e] & 0xFFFFu);
+                        const uint32_t x1 = first ? (xw[e] >> 16) : (yw[e] >> 16);
+                        const uint32_t y1 = first ? (yw[e] >> 16) : (xw[e] >> 16);
+                        if (patched)
+                            out[e] = rotate_add_fast(x0, y0, cs[2 * e], first, add[k][2 * e]) |
+                                     (rotate_add_fast(x1, y1, cs[2 * e + 1], first,
+                                                      add[k][2 * e + 1]) << 16);
+                        else
+                            out[e] = rotate_one(x0, y0, cs[2 * e], first, 0.0f) |
+                                     (rotate_one(x1, y1, cs[2 * e + 1], first, 0.0f) << 16);
+                    }
+                } else if (patched) {
+#pragma unroll
+                    for (int e = 0; e < P::CPT / 2; ++e)
+                        out[e] = bf16_rne(bf16_lo(xw[e]) + add[k][2 * e]) |
+                                 (bf16_rne(bf16_hi(xw[e]) + add[k][2 * e + 1]) << 16);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < P::CPT / 2; ++e)
+                        out[e] = xw[e];
+                }
+                char *dp = dst_base + d[k] * dst_ss + cc * 2;
+                if (P::CPT == 4)
+                    __stcs(reinterpret_cast<uint2 *>(dp), make_uint2(out[0], out[P::CPT / 2 - 1]));
+                else
+                    __stcs(reinterpret_cast<unsigned int *>(dp), out[0]);
+            }
         }
     }
     cp_async_wait<0>();
@@ -288,7 +330,8 @@ patch_chunk_kernel(const __grid_constant__ RelocParams p)
 template <class P>
 static size_t patch_smem_bytes()
 {
-    return (size_t)P::NS * P::G * P::ROW_BYTES + (size_t)P::NS * 2 * P::G * P::MMAX * sizeof(float);
+    return (size_t)P::NS * P::G * P::ROW_BYTES +
+           (size_t)P::NS * P::NCH * P::G * P::MMAX * sizeof(float);
 }
 
 template <class P, bool RELOC>
@@ -299,7 +342,7 @@ static cudaError_t launch_patch_geo(const RelocParams &p, cudaStream_t stream)
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    const dim3 grid((unsigned)p.num_chunks, (unsigned)p.src.num_layers);
+    const dim3 grid((unsigned)p.num_chunks, (unsigned)p.src.num_layers, P::SPLIT ? 2u : 1u);
     patch_chunk_kernel<P, RELOC><<<grid, P::NT, smem, stream>>>(p);
     return cudaGetLastError();
 }

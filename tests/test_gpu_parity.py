@@ -188,6 +188,29 @@ def test_relocate_nonfinite_inputs(orc):
     check_pool(dst, "relocate with Inf/NaN")
 
 
+@pytest.mark.parametrize("shape", ["mla", "gqa"])
+def test_fused_patch_nonfinite_inputs(orc, shape):
+    wl, src, dst, dev = _reloc_case(shape, 265, num_reqs=1, chunks=2, lo=40, hi=60,
+                                    deltas=[-555, 4321])
+    specials = [0x7F80, 0xFF80, 0x7FC0, 0x7F81, 0x7F80]
+    for k, b in enumerate(specials):
+        s = int(wl.src_slots[k])
+        col = (3 + 17 * k) % (src.H * src.d)
+        src.orc.rot[1, s, col] = b
+        src.rot_view[1, s, col] = torch.tensor(int(np.array(b, np.uint16).view(np.int16)),
+                                              dtype=torch.int16).view(torch.bfloat16)
+    m = 8
+    widths = (src.cd, src.H * src.d)
+    us = [synth.f32_normal((L, wl.total_tokens, m), 266 + i, std=0.02) for i in range(2)]
+    vs = [synth.f32_normal((L, wl.num_chunks, widths[i], m), 268 + i, std=0.02)
+          for i in range(2)]
+    ud, vd = [x.cuda() for x in us], [x.cuda() for x in vs]
+    assert _run_relocate(wl, src, dst, dev, patch=kv.patch_desc(m, ud, vd)) == kv.KV_OK
+    _oracle_relocate(orc, wl, src, dst,
+                     O.Patch(m, [x.numpy() for x in us], [x.numpy() for x in vs]))
+    check_pool(dst, f"fused patch with Inf/NaN ({shape})", copy_exact=False)
+
+
 # ---------------------------------------------------------------------------
 # Splice
 # ---------------------------------------------------------------------------

@@ -138,6 +138,23 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def ulp_stats(got: np.ndarray, want: np.ndarray) -> dict:
+    """Compare bf16 bit patterns as the parity tests do: exact, within 1 ulp,
+    and beyond (more than 1 ulp AND more than 1e-6 apart); NaN must meet NaN."""
+    g, w = got.astype(np.int64).ravel(), want.astype(np.int64).ravel()
+    og = np.where(g & 0x8000, 0x8000 - (g & 0x7FFF), 0x8000 + g)
+    ow = np.where(w & 0x8000, 0x8000 - (w & 0x7FFF), 0x8000 + w)
+    gf = (g.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    wf = (w.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    nan = np.isnan(gf) | np.isnan(wf)
+    dist = np.abs(og - ow)
+    with np.errstate(invalid="ignore"):
+        far = (dist > 1) & ~(np.abs(gf - wf) <= 1e-6)
+    far = np.where(nan, np.isnan(gf) != np.isnan(wf), far)
+    return {"exact": int((dist == 0).sum()), "one_ulp": int((dist == 1).sum()),
+            "beyond": int(far.sum()), "values": int(dist.size)}
+
+
 def dist_info():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -225,19 +242,11 @@ def check_relocate_sample(st, orc, n_rows: int = 3000, seed: int = 7) -> dict:
     drows = st["dst"][li, torch.from_numpy(dslot).cuda()].cpu()
     sb, db = synth.bits(srows), synth.bits(drows)
     copy_bad = int((sb[:, :512] != db[:, :512]).any(axis=1).sum())
-    exact = one = beyond = 0
-    for i in range(n_rows):
-        want = orc.rotate_bf16(sb[i, 512:], int(wl.delta[chunk[i]]), st["cfg"]["base"])
-        g = db[i, 512:].astype(np.int64)
-        w = want.astype(np.int64)
-        og = np.where(g & 0x8000, 0x8000 - (g & 0x7FFF), 0x8000 + g)
-        ow = np.where(w & 0x8000, 0x8000 - (w & 0x7FFF), 0x8000 + w)
-        dist = np.abs(og - ow)
-        exact += int((dist == 0).sum())
-        one += int((dist == 1).sum())
-        beyond += int((dist > 1).sum())
-    return {"rows": n_rows, "copy_rows_differing": copy_bad, "rot_exact": exact,
-            "rot_one_ulp": one, "rot_beyond": beyond}
+    want = np.stack([orc.rotate_bf16(sb[i, 512:], int(wl.delta[chunk[i]]), st["cfg"]["base"])
+                     for i in range(n_rows)])
+    r = ulp_stats(db[:, 512:], want)
+    return {"rows": n_rows, "copy_rows_differing": copy_bad, "rot_exact": r["exact"],
+            "rot_one_ulp": r["one_ulp"], "rot_beyond": r["beyond"]}
 
 
 def cpu_baseline_relocate(orc, cfg=RELOC_MLA, chunks: int = 3, seed: int = 4242,
@@ -483,13 +492,9 @@ def check_splice_sample(st, orc, n_rows: int = 2000, seed: int = 11) -> dict:
     got = synth.bits(st["pool"][li, si].cpu())
     wc, wr = np.stack(want_c), np.stack(want_r)
     copy_bad = int((got[:, :512] != wc).any(axis=1).sum())
-    g, w = got[:, 512:].astype(np.int64), wr.astype(np.int64)
-    og = np.where(g & 0x8000, 0x8000 - (g & 0x7FFF), 0x8000 + g)
-    ow = np.where(w & 0x8000, 0x8000 - (w & 0x7FFF), 0x8000 + w)
-    dist = np.abs(og - ow)
+    r = ulp_stats(got[:, 512:], wr)
     return {"rows": len(have_idx), "copy_rows_differing": copy_bad,
-            "rot_exact": int((dist == 0).sum()), "rot_one_ulp": int((dist == 1).sum()),
-            "rot_beyond": int((dist > 1).sum())}
+            "rot_exact": r["exact"], "rot_one_ulp": r["one_ulp"], "rot_beyond": r["beyond"]}
 
 
 def run_splice_mla_128k(args, rank, world, local):
@@ -673,14 +678,11 @@ def check_reloc_gqa_sample(st, orc, n_rows: int = 300, seed: int = 13) -> dict:
         got_k = synth.bits(st["dst_k"][l, ds].cpu())
         for got, want, key in ((got_v, dst.copy[0, 0], "copy_beyond"),
                                (got_k, dst.rot[0, 0], "rot_beyond")):
-            g, w = got.astype(np.int64), want.astype(np.int64)
-            og = np.where(g & 0x8000, 0x8000 - (g & 0x7FFF), 0x8000 + g)
-            ow = np.where(w & 0x8000, 0x8000 - (w & 0x7FFF), 0x8000 + w)
-            dist = np.abs(og - ow)
-            worst[key] += int((dist > 1).sum())
-            worst["exact"] += int((dist == 0).sum())
-            worst["one_ulp"] += int((dist == 1).sum())
-            worst["values"] += dist.size
+            r = ulp_stats(got, want)
+            worst[key] += r["beyond"]
+            worst["exact"] += r["exact"]
+            worst["one_ulp"] += r["one_ulp"]
+            worst["values"] += r["values"]
     worst["rows"] = n_rows
     return worst
 

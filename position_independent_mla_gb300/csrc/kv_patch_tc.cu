@@ -1,0 +1,378 @@
+// kv_patch_tc.cu -- the rank-m patch on the 5th-generation tensor cores
+// (tcgen05), fused with the relocation, for GQA rows (K and V of 8 x 128).
+//
+// Kamera §2: KV^(B|A) = R(δ)·KV(B|∅) + U_m V_mᵀ.  For one (chunk, layer,
+// channel) the patch is the product of U (rows x m) and V (cols x m)ᵀ, a
+// dense contraction with a short inner dimension (m <= 16).  One block of
+// 128 threads owns one head (128 columns) of one channel of one (chunk,
+// layer) and walks the chunk in tiles of 128 rows, thread = row = tensor
+// memory lane:
+//   * each thread starts loading its row's 256 bytes into registers at once
+//     (they fly while the patch is being formed), reads its U row (64
+//     contiguous bytes), splits it into bf16 high and low parts (x ~ hi + lo
+//     to ~16 bits) and stores them as K-major core matrices (8 rows x 16 B);
+//   * V's head slice was split the same way once per block; three
+//     tcgen05.mma kind::f16 (hi·hi, hi·lo, lo·hi) accumulate the 128 x 128
+//     fp32 product in tensor memory;
+//   * each thread reads its row of the product 16 columns at a time with
+//     tcgen05.ld and holds both halves of every rotary pair, so it forms
+//     rnd(R(δ)·x + patch) (or rnd(x + patch) for the verbatim channel) for
+//     the whole row and stores it with 16-byte writes.
+// Four blocks share an SM.  The wait for the MMAs is a bounded poll of an
+// mbarrier; tensor memory is released on every path.
+#include <cuda_bf16.h>
+
+#include "kv_launch.h"
+#include "kv_tiles.cuh"
+
+namespace kvr {
+namespace tc {
+
+constexpr int M = 128;                // rows per tile (MMA M) = threads per block
+constexpr int NB = 128;               // columns per block (MMA N): one rotary head
+constexpr int KP = 16;                // padded rank (MMA K for 16-bit inputs)
+constexpr int NT = M;
+constexpr int WIDTH = 1024;           // channel width (8 heads x 128)
+constexpr int HALF = NB / 2;          // frequencies per head
+constexpr int SLICES = WIDTH / NB;
+constexpr int A_BYTES = M * KP * 2;   // one of hi / lo
+constexpr int B_BYTES = NB * KP * 2;
+constexpr int ROW_VECS = NB * 2 / 16; // 16-byte pieces of a row slice
+constexpr uint32_t TMEM_COLS = NB;    // fp32 accumulator columns
+constexpr int64_t MMA_WAIT_NS = 1000000000ll;
+
+// Byte offset of element (r, k) in a K-major operand made of core matrices
+// of 8 rows x 16 bytes: core matrices are 128 B apart along K and 256 B
+// apart along M / N (the LBO / SBO of the descriptor below).
+__device__ __forceinline__ uint32_t kmajor_off(int r, int k)
+{
+    return (uint32_t)((r >> 3) * 256 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// Shared-memory matrix descriptor: no swizzle, LBO = 128 B, SBO = 256 B.
+__device__ __forceinline__ uint64_t smem_desc(const void *p)
+{
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+    return (uint64_t)((a & 0x3FFFFu) >> 4) | ((uint64_t)(128u >> 4) << 16) |
+           ((uint64_t)(256u >> 4) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NB >> 3) << 17) |
+                            ((uint32_t)(M >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc)
+{
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+                 "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 "selp.b32 %0, 1, 0, p;\n}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for an mbarrier phase (wall-time limit plus a poll cap).
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t limit_ns)
+{
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 0; it < (1u << 26); ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((int64_t)(global_ns() - t0) > limit_ns)
+            return false;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Split 8 fp32 values (k .. k+7 of one row) into bf16 high / low parts and
+// store them as one 16-byte core-matrix row each.
+__device__ __forceinline__ void split_store8(const float *v, unsigned char *hi, unsigned char *lo)
+{
+    uint32_t h[4], w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]);
+        const __nv_bfloat16 h1 = __float2bfloat16_rn(v[2 * e + 1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(v[2 * e] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(v[2 * e + 1] - __bfloat162float(h1));
+        h[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        w[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    *reinterpret_cast<uint4 *>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4 *>(lo) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Load one rank-m factor row (m <= 16 floats, 16-byte aligned), zero-padded to KP.
+__device__ __forceinline__ void load_factor_row(const float *src, int m, float (&v)[KP])
+{
+#pragma unroll
+    for (int r = 0; r < KP; r += 4) {
+        float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < m)
+            q = __ldg(reinterpret_cast<const float4 *>(src + r));
+        v[r] = q.x;
+        v[r + 1] = q.y;
+        v[r + 2] = q.z;
+        v[r + 3] = q.w;
+    }
+}
+
+template <bool RELOC>
+__global__ void __launch_bounds__(NT, 4) patch_tc_kernel(const __grid_constant__ RelocParams p)
+{
+    __shared__ __align__(128) unsigned char a_hi[A_BYTES], a_lo[A_BYTES];
+    __shared__ __align__(128) unsigned char b_hi[B_BYTES], b_lo[B_BYTES];
+    __shared__ float4 cs_s[HALF]; // (c1, c2, s1, s2) per frequency
+    __shared__ __align__(8) uint64_t s_mbar;
+    __shared__ uint32_t s_tmem;
+    __shared__ int32_t s_ok;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    // the blocks of one (chunk, layer) are adjacent in launch order
+    const int c = blockIdx.x / (2 * SLICES), l = blockIdx.y;
+    const int ch = (blockIdx.x / SLICES) % 2;
+    const int col0 = (blockIdx.x % SLICES) * NB;
+    if (blockIdx.x == 0 && l == 0 && tid == 0) {
+        if (p.tok_off[0] != 0 || p.tok_off[p.num_chunks] != p.total_tokens)
+            set_status(p.status, kStatusOutOfRange);
+    }
+    const int64_t t0 = p.tok_off[c];
+    const int64_t n = max((int64_t)0, (int64_t)p.tok_off[c + 1] - t0);
+    const int32_t req = p.chunk_req[c];
+    const bool req_ok = req >= 0 && req < p.num_reqs;
+    const int32_t *bt = p.block_tables + (int64_t)(req_ok ? req : 0) * p.max_blocks;
+    const int64_t pos0 = p.chunk_dst_pos[c];
+    const bool rotate = RELOC && ch == 1 && p.delta[c] != 0;
+    const bool patched = p.patch.u[ch] != nullptr;
+    if (!RELOC && !patched)
+        return; // in place and nothing to add: the rows stay as they are
+    const int m = p.patch.m;
+    const PoolView &sp = RELOC ? p.src : p.dst;
+    const char *src_base = (ch == 0 ? sp.copy + (int64_t)l * sp.copy_ls
+                                    : sp.rot + (int64_t)l * sp.rot_ls) + col0 * 2;
+    const int64_t src_ss = ch == 0 ? sp.copy_ss : sp.rot_ss;
+    char *dst_base = (ch == 0 ? p.dst.copy + (int64_t)l * p.dst.copy_ls
+                              : p.dst.rot + (int64_t)l * p.dst.rot_ls) + col0 * 2;
+    const int64_t dst_ss = ch == 0 ? p.dst.copy_ss : p.dst.rot_ss;
+
+    // --- once per block: V's head slice as the B operand, cos/sin, barrier, TMEM
+    if (patched) {
+        float v[KP];
+        load_factor_row(p.patch.v[ch] + (int64_t)l * p.patch.v_ls[ch] +
+                            (int64_t)c * p.patch.v_cs[ch] +
+                            (int64_t)(col0 + tid) * p.patch.v_cols[ch],
+                        m, v);
+        split_store8(v, b_hi + kmajor_off(tid, 0), b_lo + kmajor_off(tid, 0));
+        split_store8(v + 8, b_hi + kmajor_off(tid, 8), b_lo + kmajor_off(tid, 8));
+    }
+    if (rotate && tid < HALF)
+        cs_s[tid] = p.table[(int64_t)c * HALF + tid];
+    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_mbar);
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+        s_ok = 1;
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         (uint32_t)__cvta_generic_to_shared(&s_tmem)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = s_tmem;
+    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16); // my lane quarter
+
+    const int64_t ntiles = (n + M - 1) / M;
+    uint32_t phase = 0;
+    for (int64_t t = 0; t < ntiles; ++t) {
+        // my row: slots, then its 256 bytes start flying into registers
+        const int64_t i = t * M + tid;
+        int64_t src = -1, dst = -1;
+        if (i < n) {
+            if (req_ok)
+                dst = slot_of(bt, p.max_blocks, p.dst.block, p.dst.num_blocks, pos0 + i);
+            if (RELOC) {
+                const int64_t sl = p.src_slots[t0 + i];
+                src = (sl >= 0 && sl < p.src.num_slots) ? sl : -1;
+            } else {
+                src = dst;
+            }
+            if (src < 0 || dst < 0) {
+                set_status(p.status, kStatusOutOfRange);
+                src = dst = -1;
+            }
+        }
+        uint4 xv[ROW_VECS];
+        if (src >= 0) {
+            const uint4 *xs = reinterpret_cast<const uint4 *>(src_base + src * src_ss);
+#pragma unroll
+            for (int v = 0; v < ROW_VECS; ++v)
+                xv[v] = xs[v];
+        } else {
+#pragma unroll
+            for (int v = 0; v < ROW_VECS; ++v)
+                xv[v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (patched) {
+            // A operand: my U row split into bf16 hi / lo (zeros for an empty row)
+            float u[KP];
+            if (src >= 0) {
+                load_factor_row(p.patch.u[ch] + (int64_t)l * p.patch.u_ls[ch] +
+                                    (t0 + i) * p.patch.u_ts[ch],
+                                m, u);
+            } else {
+#pragma unroll
+                for (int r = 0; r < KP; ++r)
+                    u[r] = 0.0f;
+            }
+            split_store8(u, a_hi + kmajor_off(tid, 0), a_lo + kmajor_off(tid, 0));
+            split_store8(u + 8, a_hi + kmajor_off(tid, 8), a_lo + kmajor_off(tid, 8));
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            fence_before();
+            __syncthreads(); // A complete; the previous tile's accumulator reads are done
+            if (tid == 0) {
+                fence_after();
+                mma_bf16(tmem, smem_desc(a_hi), smem_desc(b_hi), 0u);
+                mma_bf16(tmem, smem_desc(a_hi), smem_desc(b_lo), 1u);
+                mma_bf16(tmem, smem_desc(a_lo), smem_desc(b_hi), 1u);
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                             : "memory");
+                if (!mbar_wait(bar, phase, MMA_WAIT_NS)) {
+                    set_status(p.status, kStatusTimeout);
+                    // give the MMAs one more bounded wait before the memory is released
+                    mbar_wait(bar, phase, MMA_WAIT_NS);
+                    s_ok = 0;
+                }
+            }
+            phase ^= 1u;
+            __syncthreads();
+            fence_after();
+            if (!s_ok)
+                break;
+        }
+        // my output row, 16 columns (or 16 rotary pairs) at a time
+        const uint32_t *xw = reinterpret_cast<const uint32_t *>(xv);
+        uint4 *dp = reinterpret_cast<uint4 *>(dst_base + (dst >= 0 ? dst : 0) * dst_ss);
+        if (rotate) {
+#pragma unroll
+            for (int f0 = 0; f0 < HALF; f0 += 16) {
+                uint32_t a1[16], a2[16];
+                if (patched) {
+                    tmem_ld16(t_row + (uint32_t)f0, a1);
+                    tmem_ld16(t_row + (uint32_t)(f0 + HALF), a2);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        a1[e] = a2[e] = 0u;
+                }
+                uint32_t o1[8], o2[8];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    // (x1, x2) = (x[j], x[j+64]) turned by δθ_j; cos = c1 + c2,
+                    // sin = s1 + s2 with c1, s1 short enough for exact products
+                    const float4 q = cs_s[f0 + e];
+                    const uint32_t w1 = xw[(f0 + e) >> 1], w2 = xw[(f0 + HALF + e) >> 1];
+                    const float x1 = (e & 1) ? bf16_hi(w1) : bf16_lo(w1);
+                    const float x2 = (e & 1) ? bf16_hi(w2) : bf16_lo(w2);
+                    const float r1 = fmaf(x1, q.x, -(x2 * q.z)) +
+                                     (fmaf(x1, q.y, -(x2 * q.w)) + __uint_as_float(a1[e]));
+                    const float r2 = fmaf(x2, q.x, x1 * q.z) +
+                                     (fmaf(x2, q.y, x1 * q.w) + __uint_as_float(a2[e]));
+                    const uint32_t b1 = bf16_rne(r1), b2 = bf16_rne(r2);
+                    if (e & 1) {
+                        o1[e >> 1] |= b1 << 16;
+                        o2[e >> 1] |= b2 << 16;
+                    } else {
+                        o1[e >> 1] = b1;
+                        o2[e >> 1] = b2;
+                    }
+                }
+                if (dst >= 0) {
+                    __stcs(dp + f0 / 8, make_uint4(o1[0], o1[1], o1[2], o1[3]));
+                    __stcs(dp + f0 / 8 + 1, make_uint4(o1[4], o1[5], o1[6], o1[7]));
+                    __stcs(dp + (f0 + HALF) / 8, make_uint4(o2[0], o2[1], o2[2], o2[3]));
+                    __stcs(dp + (f0 + HALF) / 8 + 1, make_uint4(o2[4], o2[5], o2[6], o2[7]));
+                }
+            }
+        } else {
+#pragma unroll
+            for (int c16 = 0; c16 < NB; c16 += 16) {
+                uint32_t a[16];
+                if (patched) {
+                    tmem_ld16(t_row + (uint32_t)c16, a);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        a[e] = 0u;
+                }
+                uint32_t o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t w = xw[c16 / 2 + e];
+                    o[e] = bf16_rne(bf16_lo(w) + __uint_as_float(a[2 * e])) |
+                           (bf16_rne(bf16_hi(w) + __uint_as_float(a[2 * e + 1])) << 16);
+                }
+                if (dst >= 0) {
+                    __stcs(dp + c16 / 8, make_uint4(o[0], o[1], o[2], o[3]));
+                    __stcs(dp + c16 / 8 + 1, make_uint4(o[4], o[5], o[6], o[7]));
+                }
+            }
+        }
+    }
+    fence_before();
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+}
+
+} // namespace tc
+
+bool patch_tc_supported(const RelocParams &p, RowKind kind)
+{
+    return kind == RowKind::Gqa && p.patched && p.patch.m <= tc::KP &&
+           p.src.num_layers <= 65535;
+}
+
+cudaError_t launch_patch_tc(const RelocParams &p, cudaStream_t stream)
+{
+    if (p.num_chunks == 0)
+        return cudaSuccess;
+    if ((int64_t)p.num_chunks * 2 * tc::SLICES > 0x7FFFFFFFll)
+        return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)(p.num_chunks * 2 * tc::SLICES), (unsigned)p.src.num_layers);
+    if (p.in_place)
+        tc::patch_tc_kernel<false><<<grid, tc::NT, 0, stream>>>(p);
+    else
+        tc::patch_tc_kernel<true><<<grid, tc::NT, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+} // namespace kvr

@@ -72,18 +72,19 @@ __device__ __forceinline__ uint32_t bf16_round(float hi, float lo)
 // added to et.  (hi, lo) then holds the rotated value to about 2^-38 of
 // |x|+|y|, and one tie-aware rounding gives the bf16 nearest to it.
 
-// Output of this lane for one pair: `first` selects x*cos - y*sin (the lane
-// holding the first half of the head) or x*sin + y*cos (second half).
-// `add` is an fp32 term (the rank-m patch, or 0) added before rounding.
-__device__ __forceinline__ uint32_t rotate_one(uint32_t xb, uint32_t yb, float4 cs, bool first,
-                                               float add)
+// The exact path: the rotated value to ~2^-38 of |x|+|y| as (hi, lo) and one
+// tie-aware rounding.  `first` selects x*cos - y*sin (the lane holding the
+// first half of the head) or x*sin + y*cos (second half); `add` is an fp32
+// term (the rank-m patch, or 0) added before rounding.
+static __device__ __noinline__ uint32_t rotate_one_exact(uint32_t xb, uint32_t yb, float4 cs, bool first,
+                                                  float add)
 {
     const float x = __uint_as_float(xb << 16), y = __uint_as_float(yb << 16);
     float hi, lo;
     if (bf16_finite(xb) && bf16_finite(yb)) {
         float p, q, u;
         if (first) {
-            p = x * cs.x; // exact
+            p = x * cs.x;    // exact
             q = -(y * cs.z); // exact
             u = fmaf(x, cs.y, -(y * cs.w));
         } else {
@@ -103,6 +104,34 @@ __device__ __forceinline__ uint32_t rotate_one(uint32_t xb, uint32_t yb, float4 
     float s, e;
     two_sum(hi, lo + add, s, e);
     return bf16_round(s, e);
+}
+
+// Same result, cheaply: with exact leading products, t + (u + add) is the
+// rotated value to within a few fp32 ulps, so round-to-nearest-even of it is
+// already the correctly rounded bf16 unless it lies within 4 fp32 ulps of a
+// bf16 rounding boundary, is not finite, or comes out of heavy cancellation
+// (|result| below 2^-12 (|x|+|y|)).  Those rare cases (about 1e-4 of values)
+// take the exact path.
+__device__ __forceinline__ uint32_t rotate_one(uint32_t xb, uint32_t yb, float4 cs, bool first,
+                                               float add)
+{
+    const float x = __uint_as_float(xb << 16), y = __uint_as_float(yb << 16);
+    float t, u;
+    if (first) {
+        t = fmaf(x, cs.x, -(y * cs.z));
+        u = fmaf(x, cs.y, -(y * cs.w));
+    } else {
+        t = fmaf(x, cs.z, y * cs.x);
+        u = fmaf(x, cs.w, y * cs.y);
+    }
+    const float s = t + (u + add);
+    const uint32_t b = __float_as_uint(s);
+    const bool near_tie = ((b & 0xFFFFu) - 0x7FFCu) <= 8u;
+    const bool special = (b & 0x7F800000u) == 0x7F800000u;
+    const bool cancels = fabsf(s) < 2.44140625e-4f * (fabsf(x) + fabsf(y)); // 2^-12
+    if (near_tie || special || cancels)
+        return rotate_one_exact(xb, yb, cs, first, add);
+    return (b + 0x7FFFu + ((b >> 16) & 1u)) >> 16;
 }
 
 // Patched values are held to 1 bf16 ulp (the fp32 patch sum carries its
@@ -152,10 +181,10 @@ __device__ __forceinline__ uint32_t add_round(uint32_t xb, float add)
 
 // Rotate one 16-byte vector (8 bf16) of a head.  `mine` is this lane's
 // vector, `other` its partner's (the same 8 frequencies in the other half),
-// `first` tells whether `mine` lies in the first half.  cs points at the 8
-// table entries of these frequencies; add[8] is the patch term (or zeros).
+// `first` tells whether `mine` lies in the first half.  The table entry of
+// element e is cs[e * cs_step]; add[8] is the patch term (or zeros).
 __device__ __forceinline__ uint4 rotate_vec(uint4 mine, uint4 other, bool first,
-                                            const float4 *cs, const float *add)
+                                            const float4 *cs, int cs_step, const float *add)
 {
     const uint32_t m[4] = {mine.x, mine.y, mine.z, mine.w};
     const uint32_t o[4] = {other.x, other.y, other.z, other.w};
@@ -164,8 +193,10 @@ __device__ __forceinline__ uint4 rotate_vec(uint4 mine, uint4 other, bool first,
     for (int k = 0; k < 4; ++k) {
         const uint32_t xw = first ? m[k] : o[k];
         const uint32_t yw = first ? o[k] : m[k];
-        const uint32_t r0 = rotate_one(xw & 0xFFFFu, yw & 0xFFFFu, cs[2 * k], first, add[2 * k]);
-        const uint32_t r1 = rotate_one(xw >> 16, yw >> 16, cs[2 * k + 1], first, add[2 * k + 1]);
+        const uint32_t r0 =
+            rotate_one(xw & 0xFFFFu, yw & 0xFFFFu, cs[(2 * k) * cs_step], first, add[2 * k]);
+        const uint32_t r1 =
+            rotate_one(xw >> 16, yw >> 16, cs[(2 * k + 1) * cs_step], first, add[2 * k + 1]);
         out[k] = r0 | (r1 << 16);
     }
     return make_uint4(out[0], out[1], out[2], out[3]);

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const
     __shared__ int64_t s_tok[G::T];
     __shared__ int32_t s_chunk[G::T];
     __shared__ int32_t s_ident[G::T];
-    __shared__ float4 s_cs[G::T][G::kHalf];
+    __shared__ float4 s_cs[G::T][G::kCsRow];
 
     const int tid = threadIdx.x;
     const int64_t tile0 = (int64_t)blockIdx.x * G::T;
@@ -112,9 +112,9 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const
     if (!p.in_place) {
         for (int i = tid; i < G::T * G::kHalf; i += kThreads) {
             const int r = i / G::kHalf, j = i % G::kHalf;
-            s_cs[r][j] = (s_src[r] >= 0 && !s_ident[r])
-                             ? p.table[(int64_t)s_chunk[r] * G::kHalf + j]
-                             : make_float4(1.f, 0.f, 0.f, 0.f);
+            s_cs[r][G::cs_index(j)] = (s_src[r] >= 0 && !s_ident[r])
+                                          ? p.table[(int64_t)s_chunk[r] * G::kHalf + j]
+                                          : make_float4(1.f, 0.f, 0.f, 0.f);
         }
         __syncthreads();
     }
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const
         TileRegs<G> regs;
         load_tile<G>(from, s_src, regs);
         pa.layer = l;
-        store_tile<G, PATCH>(to, s_dst, regs, &s_cs[0][0], G::kHalf, s_ident, pa);
+        store_tile<G, PATCH>(to, s_dst, regs, &s_cs[0][0], G::kCsRow, s_ident, pa);
     }
 }
 

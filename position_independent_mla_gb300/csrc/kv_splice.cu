@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
         }
     }
     for (int j = tid; j < G::kHalf; j += kThreads)
-        s_cs[j] = p.table[(int64_t)q * G::kHalf + j];
+        s_cs[G::cs_index(j)] = p.table[(int64_t)q * G::kHalf + j];
     __syncthreads();
 
     const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;

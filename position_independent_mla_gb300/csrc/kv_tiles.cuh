@@ -27,6 +27,11 @@ struct Geo {
     static constexpr int kRotItems = T * kRotW;
     static constexpr int kCopyPer = (kCopyItems + kThreads - 1) / kThreads;
     static constexpr int kRotPer = (kRotItems + kThreads - 1) / kThreads;
+    // cos/sin rows in shared memory are stored transposed -- entry e of the
+    // 8 frequencies of vector group vv at e*HV + vv -- and padded by 4
+    // entries, so the lanes of a warp read them without bank conflicts.
+    static constexpr int kCsRow = kHalf + 4;
+    static __device__ __forceinline__ int cs_index(int f) { return (f % 8) * HV + f / 8; }
     static_assert(32 % (2 * HV) == 0, "a rotary head's vectors must tile a warp");
     static_assert(kThreads % (2 * HV) == 0, "partner lanes must stay in one item round");
 };
@@ -131,8 +136,9 @@ __device__ __forceinline__ void patch_terms(const PatchView &pv, int ch, int l, 
 }
 
 // Write a loaded tile: verbatim vectors as they are (plus the patch),
-// rotary vectors turned by the row's cos/sin (cs + row*cs_row_stride) unless
-// the row is marked identity.
+// rotary vectors turned by the row's cos/sin (a transposed table row at
+// cs + row*cs_row_stride, see Geo::cs_index) unless the row is marked
+// identity.
 template <class G, bool PATCH>
 __device__ __forceinline__ void store_tile(const RowsAt &at, const int64_t *idx,
                                            const TileRegs<G> &regs, const float4 *cs,
@@ -182,7 +188,8 @@ __device__ __forceinline__ void store_tile(const RowsAt &at, const int64_t *idx,
                 if (ident[row])
                     out = patched ? add_vec(regs.r[k], add) : regs.r[k];
                 else
-                    out = rotate_vec(regs.r[k], partner, first, cs + row * cs_row_stride + fb, add);
+                    out = rotate_vec(regs.r[k], partner, first,
+                                     cs + row * cs_row_stride + fb / 8, G::HV, add);
                 st_stream(const_cast<char *>(at.rbase) + s * at.rstride + w * 16, out);
             }
         }

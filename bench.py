@@ -386,6 +386,44 @@ def run_relocate_mla(args, rank, world, local):
     return out
 
 
+def check_reloc_mla_patch_sample(st, u, v, m, orc, n_rows: int = 300, seed: int = 17) -> dict:
+    """Sampled parity at full size for the patched MLA relocation: random
+    (token, layer) rows, each checked against the oracle's fused relocation +
+    patch on a one-token problem built from that row's source values and its
+    U / V factors (one 576-wide factor pair split at column 512)."""
+    import oracle as O
+
+    wl, L, base = st["wl"], st["L"], st["cfg"]["base"]
+    rng = np.random.default_rng(seed)
+    out = {"copy_beyond": 0, "rot_beyond": 0, "exact": 0, "one_ulp": 0, "values": 0}
+    for _ in range(n_rows):
+        t = int(rng.integers(wl.total_tokens))
+        l = int(rng.integers(L))
+        c = int(np.searchsorted(wl.tok_off, t, side="right") - 1)
+        pos = int(wl.chunk_dst_pos[c]) + t - int(wl.tok_off[c])
+        ds = int(wl.block_tables[wl.chunk_req[c], pos // 64]) * 64 + pos % 64
+        row = synth.bits(st["src"][l, int(wl.src_slots[t])].cpu())
+        sc, sr = np.zeros((1, 64, 512), np.uint16), np.zeros((1, 64, 64), np.uint16)
+        sc[0, 0], sr[0, 0] = row[:512], row[512:]
+        src = O.Pool(sc, sr, 64, 1, 64, base)
+        dst = O.Pool(np.zeros((1, 64, 512), np.uint16), np.zeros((1, 64, 64), np.uint16), 64, 1,
+                     64, base)
+        ut = u[l, t].cpu().numpy().reshape(1, 1, m)
+        vc = v[l, c].cpu().numpy().reshape(1, 1, 576, m)
+        assert orc.relocate(src, dst, [0, 1], [0], [0], [0], [int(wl.delta[c])], [[0]],
+                            O.Patch(m, [ut, ut], [vc[:, :, :512], vc[:, :, 512:]])) == O.OK
+        got = synth.bits(st["dst"][l, ds].cpu())
+        for g, want, key in ((got[:512], dst.copy[0, 0], "copy_beyond"),
+                             (got[512:], dst.rot[0, 0], "rot_beyond")):
+            r = ulp_stats(g, want)
+            out[key] += r["beyond"]
+            out["exact"] += r["exact"]
+            out["one_ulp"] += r["one_ulp"]
+            out["values"] += r["values"]
+    out["rows"] = n_rows
+    return out
+
+
 def run_relocate_mla_patch(args, rank, world, local):
     """The headline relocation with Kamera's rank-8 patch fused: one factor
     pair over the 576-wide MLA row (c_KV and k_pe both patched), fp32
@@ -436,7 +474,7 @@ def run_relocate_mla_patch(args, rank, world, local):
     bytes_launch = T * (L * 2 * MLA_ROW_BYTES + 4) + T * L * m * 4 + wl.num_chunks * L * 576 * m * 4
     peak, peak_kind = hbm_peak()
     achieved = bytes_launch / (kern_ms * 1e-3) / 1e9
-    return {
+    out = {
         "metric": "relocated KV tokens/s (all layers)", "value": T * world / (step_ms * 1e-3),
         "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -445,10 +483,14 @@ def run_relocate_mla_patch(args, rank, world, local):
                    "tokens_per_step_per_gpu": T, "layers": L},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
-                     "kernel": "patch_chunk_kernel<MLA, relocate>", "kernel_ms": kern_ms,
-                     "algorithmic_bytes_per_launch": bytes_launch},
+                     "kernel": "patch_tc_kernel (c_KV: 256-column slices; k_pe: 64)",
+                     "kernel_ms": kern_ms, "algorithmic_bytes_per_launch": bytes_launch},
         "clocks": clk, "gpu_launches": launches,
     }
+    if args.check and rank == 0:
+        import oracle as O
+        out["parity_sample"] = check_reloc_mla_patch_sample(st, u, v, m, O.get())
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -850,7 +892,7 @@ def run_relocate_gqa_patch(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": recorded_traffic("relocate_gqa_patch"),
-                     "kernel": "patch_chunk_kernel<GQA, relocate>", "kernel_ms": kern_ms,
+                     "kernel": "patch_tc_kernel (256-column slices, two heads)", "kernel_ms": kern_ms,
                      "algorithmic_bytes_per_launch": bytes_per_launch,
                      "patch_tflops": flops / (kern_ms * 1e-3) / 1e12},
         "e2e": {"value": T * world * K / e2e_s, "unit": "tokens/s",

@@ -207,14 +207,17 @@ kv_status relocate_impl(const kv_pool_desc *src, const kv_pool_desc *dst, int32_
     rp.in_place = in_place ? 1 : 0;
     rp.status = reinterpret_cast<uint32_t *>(w);
     KV_CUDA(mark(t_ev_start, stream));
-    if (patch_tc_supported(rp, kind))
-        KV_CUDA(launch_patch_tc(rp, stream));
-    else if (patch_chunk_supported(rp))
-        KV_CUDA(launch_patch_chunks(rp, kind, stream));
-    else
-        KV_CUDA(launch_relocate(rp, kind, stream));
+    if (patch_tc_supported(rp, kind)) {
+        KV_CUDA(launch_patch_tc(rp, kind, stream));
+        t_launches += patch_tc_launches(kind);
+    } else {
+        if (patch_chunk_supported(rp))
+            KV_CUDA(launch_patch_chunks(rp, kind, stream));
+        else
+            KV_CUDA(launch_relocate(rp, kind, stream));
+        ++t_launches;
+    }
     KV_CUDA(mark(t_ev_stop, stream));
-    ++t_launches;
     return KV_OK;
 }
 

@@ -16,9 +16,10 @@ cudaError_t launch_relocate(const RelocParams &p, RowKind kind, cudaStream_t str
 // Patched relocation / in-place patch, one block per (chunk, layer), ranks <= 16.
 bool patch_chunk_supported(const RelocParams &p);
 cudaError_t launch_patch_chunks(const RelocParams &p, RowKind kind, cudaStream_t stream);
-// The same on the tensor cores (tcgen05), GQA rows, ranks <= 16.
+// The same on the tensor cores (tcgen05), ranks <= 16.
 bool patch_tc_supported(const RelocParams &p, RowKind kind);
-cudaError_t launch_patch_tc(const RelocParams &p, cudaStream_t stream);
+cudaError_t launch_patch_tc(const RelocParams &p, RowKind kind, cudaStream_t stream);
+int patch_tc_launches(RowKind kind); // kernels one launch_patch_tc issues
 // Launches one ticketed block per tile; `blocks` = p.total_tickets.
 cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stream);
 cudaError_t launch_wait_check(uint32_t *flag, uint32_t *status, int64_t limit_ns,

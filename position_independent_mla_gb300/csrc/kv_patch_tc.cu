@@ -1,25 +1,27 @@
 // kv_patch_tc.cu -- the rank-m patch on the 5th-generation tensor cores
-// (tcgen05), fused with the relocation, for GQA rows (K and V of 8 x 128).
+// (tcgen05), fused with the relocation (or applied in place).
 //
 // Kamera §2: KV^(B|A) = R(δ)·KV(B|∅) + U_m V_mᵀ.  For one (chunk, layer,
 // channel) the patch is the product of U (rows x m) and V (cols x m)ᵀ, a
-// dense contraction with a short inner dimension (m <= 16).  One block of
-// 128 threads owns one head (128 columns) of one channel of one (chunk,
-// layer) and walks the chunk in tiles of 128 rows, thread = row = tensor
-// memory lane:
-//   * each thread starts loading its row's 256 bytes into registers at once
-//     (they fly while the patch is being formed), reads its U row (64
-//     contiguous bytes), splits it into bf16 high and low parts (x ~ hi + lo
-//     to ~16 bits) and stores them as K-major core matrices (8 rows x 16 B);
-//   * V's head slice was split the same way once per block; three
-//     tcgen05.mma kind::f16 (hi·hi, hi·lo, lo·hi) accumulate the 128 x 128
-//     fp32 product in tensor memory;
-//   * each thread reads its row of the product 16 columns at a time with
-//     tcgen05.ld and holds both halves of every rotary pair, so it forms
-//     rnd(R(δ)·x + patch) (or rnd(x + patch) for the verbatim channel) for
-//     the whole row and stores it with 16-byte writes.
-// Four blocks share an SM.  The wait for the MMAs is a bounded poll of an
-// mbarrier; tensor memory is released on every path.
+// dense contraction with a short inner dimension (m <= 16).  A block owns a
+// slice of NB columns of one channel of one (chunk, layer) and walks the
+// chunk in tiles of 128 rows.  Its threads are (row, column group): row =
+// tensor-memory lane, a group of W columns (one rotary head, W = D, for the
+// rotated channel), so a thread holds both halves of every rotary pair it
+// writes.  Per tile:
+//   * each thread loads its row's W columns into registers (they fly while
+//     the patch is being formed) and converts its share of the tile's U rows
+//     into bf16 high and low parts (x ~ hi + lo to ~16 bits), stored as
+//     K-major core matrices (8 rows x 16 B) -- once per slice, shared by all
+//     its heads;
+//   * V's slice was split the same way once per block; three tcgen05.mma
+//     kind::f16 (hi·hi, hi·lo, lo·hi) accumulate the 128 x NB fp32 product in
+//     tensor memory;
+//   * each thread reads its part of the product 16 columns at a time with
+//     tcgen05.ld, forms rnd(R(δ)·x + patch) (rotated channel) or
+//     rnd(x + patch) and stores it with 16-byte writes.
+// The wait for the MMAs is a bounded poll of an mbarrier; tensor memory is
+// released on every path.
 #include <cuda_bf16.h>
 
 #include "kv_launch.h"
@@ -28,18 +30,25 @@
 namespace kvr {
 namespace tc {
 
-constexpr int M = 128;                // rows per tile (MMA M) = threads per block
-constexpr int NB = 128;               // columns per block (MMA N): one rotary head
+constexpr int M = 128;                // rows per tile (MMA M)
 constexpr int KP = 16;                // padded rank (MMA K for 16-bit inputs)
-constexpr int NT = M;
-constexpr int WIDTH = 1024;           // channel width (8 heads x 128)
-constexpr int HALF = NB / 2;          // frequencies per head
-constexpr int SLICES = WIDTH / NB;
 constexpr int A_BYTES = M * KP * 2;   // one of hi / lo
-constexpr int B_BYTES = NB * KP * 2;
-constexpr int ROW_VECS = NB * 2 / 16; // 16-byte pieces of a row slice
-constexpr uint32_t TMEM_COLS = NB;    // fp32 accumulator columns
 constexpr int64_t MMA_WAIT_NS = 1000000000ll;
+
+// NB: columns per block (MMA N, TMEM columns); W: columns per thread;
+// D: rotary head dim of the rotated channel (D == W).
+template <int NB_, int W_>
+struct TcGeo {
+    static constexpr int NB = NB_, W = W_;
+    static constexpr int GROUPS = NB / W;          // column groups per block
+    static constexpr int NT = M * GROUPS;          // threads per block
+    static constexpr int B_BYTES = NB * KP * 2;    // one of hi / lo
+    static constexpr int VECS = W * 2 / 16;        // 16-byte pieces of my columns
+    static constexpr int HALF = W / 2;             // frequencies of my head
+    static constexpr int MIN_BLOCKS = 512 / NB < 4 ? 512 / NB : 4; // TMEM: 512 columns / SM
+    static_assert(NB == 64 || NB == 128 || NB == 256, "MMA N");
+    static_assert(W % 16 == 0 && NB % W == 0 && (GROUPS == 1 || GROUPS == 2), "groups");
+};
 
 // Byte offset of element (r, k) in a K-major operand made of core matrices
 // of 8 rows x 16 bytes: core matrices are 128 B apart along K and 256 B
@@ -58,14 +67,19 @@ __device__ __forceinline__ uint64_t smem_desc(const void *p)
 }
 
 // Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(NB >> 3) << 17) |
-                            ((uint32_t)(M >> 4) << 24);
+template <int N>
+__device__ __forceinline__ constexpr uint32_t idesc()
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
 
+template <int N>
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc)
 {
     asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-                 "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
+                 "l"(a), "l"(b), "r"(idesc<N>()), "r"(acc)
                  : "memory");
 }
 
@@ -125,14 +139,14 @@ __device__ __forceinline__ void split_store8(const float *v, unsigned char *hi, 
     *reinterpret_cast<uint4 *>(lo) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Load one rank-m factor row (m <= 16 floats, 16-byte aligned), zero-padded to KP.
-__device__ __forceinline__ void load_factor_row(const float *src, int m, float (&v)[KP])
+// Load 8 factor values (ranks k0 .. k0+7, zero past m) of one factor row.
+__device__ __forceinline__ void load_factor8(const float *row, int k0, int m, float (&v)[8])
 {
 #pragma unroll
-    for (int r = 0; r < KP; r += 4) {
+    for (int r = 0; r < 8; r += 4) {
         float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < m)
-            q = __ldg(reinterpret_cast<const float4 *>(src + r));
+        if (k0 + r < m)
+            q = __ldg(reinterpret_cast<const float4 *>(row + k0 + r));
         v[r] = q.x;
         v[r + 1] = q.y;
         v[r + 2] = q.z;
@@ -140,21 +154,28 @@ __device__ __forceinline__ void load_factor_row(const float *src, int m, float (
     }
 }
 
-template <bool RELOC>
-__global__ void __launch_bounds__(NT, 4) patch_tc_kernel(const __grid_constant__ RelocParams p)
+// Which blocks a launch covers: channels [ch0, ch0 + nch), `slices` slices
+// of NB columns each; block x = (chunk * nch + ch - ch0) * slices + slice.
+struct TcLaunch {
+    int32_t ch0, nch, slices;
+};
+
+template <class G, bool RELOC>
+__global__ void __launch_bounds__(G::NT, G::MIN_BLOCKS)
+patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
 {
     __shared__ __align__(128) unsigned char a_hi[A_BYTES], a_lo[A_BYTES];
-    __shared__ __align__(128) unsigned char b_hi[B_BYTES], b_lo[B_BYTES];
-    __shared__ float4 cs_s[HALF]; // (c1, c2, s1, s2) per frequency
+    __shared__ __align__(128) unsigned char b_hi[G::B_BYTES], b_lo[G::B_BYTES];
+    __shared__ float4 cs_s[G::HALF > 0 ? G::HALF : 1]; // (c1, c2, s1, s2) per frequency
     __shared__ __align__(8) uint64_t s_mbar;
     __shared__ uint32_t s_tmem;
     __shared__ int32_t s_ok;
 
-    const int tid = threadIdx.x, warp = tid >> 5;
-    // the blocks of one (chunk, layer) are adjacent in launch order
-    const int c = blockIdx.x / (2 * SLICES), l = blockIdx.y;
-    const int ch = (blockIdx.x / SLICES) % 2;
-    const int col0 = (blockIdx.x % SLICES) * NB;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per_chunk = tl.nch * tl.slices;
+    const int c = blockIdx.x / per_chunk, l = blockIdx.y;
+    const int ch = tl.ch0 + (blockIdx.x / tl.slices) % tl.nch;
+    const int col0 = (blockIdx.x % tl.slices) * G::NB;
     if (blockIdx.x == 0 && l == 0 && tid == 0) {
         if (p.tok_off[0] != 0 || p.tok_off[p.num_chunks] != p.total_tokens)
             set_status(p.status, kStatusOutOfRange);
@@ -170,26 +191,30 @@ __global__ void __launch_bounds__(NT, 4) patch_tc_kernel(const __grid_constant__
     if (!RELOC && !patched)
         return; // in place and nothing to add: the rows stay as they are
     const int m = p.patch.m;
+    const int row = (warp & 3) * 32 + lane; // my row of the tile = TMEM lane
+    const int grp = warp >> 2;              // my column group
+    const int cg = grp * G::W;              // its first column in the slice
     const PoolView &sp = RELOC ? p.src : p.dst;
     const char *src_base = (ch == 0 ? sp.copy + (int64_t)l * sp.copy_ls
-                                    : sp.rot + (int64_t)l * sp.rot_ls) + col0 * 2;
+                                    : sp.rot + (int64_t)l * sp.rot_ls) + (col0 + cg) * 2;
     const int64_t src_ss = ch == 0 ? sp.copy_ss : sp.rot_ss;
     char *dst_base = (ch == 0 ? p.dst.copy + (int64_t)l * p.dst.copy_ls
-                              : p.dst.rot + (int64_t)l * p.dst.rot_ls) + col0 * 2;
+                              : p.dst.rot + (int64_t)l * p.dst.rot_ls) + (col0 + cg) * 2;
     const int64_t dst_ss = ch == 0 ? p.dst.copy_ss : p.dst.rot_ss;
 
-    // --- once per block: V's head slice as the B operand, cos/sin, barrier, TMEM
+    // --- once per block: V's slice as the B operand, cos/sin, barrier, TMEM
     if (patched) {
-        float v[KP];
-        load_factor_row(p.patch.v[ch] + (int64_t)l * p.patch.v_ls[ch] +
-                            (int64_t)c * p.patch.v_cs[ch] +
-                            (int64_t)(col0 + tid) * p.patch.v_cols[ch],
-                        m, v);
-        split_store8(v, b_hi + kmajor_off(tid, 0), b_lo + kmajor_off(tid, 0));
-        split_store8(v + 8, b_hi + kmajor_off(tid, 8), b_lo + kmajor_off(tid, 8));
+        const float *vb = p.patch.v[ch] + (int64_t)l * p.patch.v_ls[ch] +
+                          (int64_t)c * p.patch.v_cs[ch] + (int64_t)col0 * p.patch.v_cols[ch];
+        for (int i = tid; i < G::NB * 2; i += G::NT) {
+            const int nn = i >> 1, k0 = (i & 1) * 8;
+            float v[8];
+            load_factor8(vb + (int64_t)nn * p.patch.v_cols[ch], k0, m, v);
+            split_store8(v, b_hi + kmajor_off(nn, k0), b_lo + kmajor_off(nn, k0));
+        }
     }
-    if (rotate && tid < HALF)
-        cs_s[tid] = p.table[(int64_t)c * HALF + tid];
+    if (rotate && tid < G::HALF)
+        cs_s[tid] = p.table[(int64_t)c * G::HALF + tid];
     const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_mbar);
     if (tid == 0) {
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
@@ -198,7 +223,7 @@ __global__ void __launch_bounds__(NT, 4) patch_tc_kernel(const __grid_constant__
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          (uint32_t)__cvta_generic_to_shared(&s_tmem)),
-                     "r"(TMEM_COLS)
+                     "r"((uint32_t)G::NB)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -206,13 +231,13 @@ __global__ void __launch_bounds__(NT, 4) patch_tc_kernel(const __grid_constant__
     __syncthreads();
     fence_after();
     const uint32_t tmem = s_tmem;
-    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16); // my lane quarter
+    const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)cg;
 
     const int64_t ntiles = (n + M - 1) / M;
     uint32_t phase = 0;
     for (int64_t t = 0; t < ntiles; ++t) {
-        // my row: slots, then its 256 bytes start flying into registers
-        const int64_t i = t * M + tid;
+        // my row: slots, then its W columns start flying into registers
+        const int64_t i = t * M + row;
         int64_t src = -1, dst = -1;
         if (i < n) {
             if (req_ok)
@@ -224,43 +249,47 @@ __global__ void __launch_bounds__(NT, 4) patch_tc_kernel(const __grid_constant__
                 src = dst;
             }
             if (src < 0 || dst < 0) {
-                set_status(p.status, kStatusOutOfRange);
+                if (grp == 0)
+                    set_status(p.status, kStatusOutOfRange);
                 src = dst = -1;
             }
         }
-        uint4 xv[ROW_VECS];
+        uint4 xv[G::VECS];
         if (src >= 0) {
             const uint4 *xs = reinterpret_cast<const uint4 *>(src_base + src * src_ss);
 #pragma unroll
-            for (int v = 0; v < ROW_VECS; ++v)
+            for (int v = 0; v < G::VECS; ++v)
                 xv[v] = xs[v];
         } else {
 #pragma unroll
-            for (int v = 0; v < ROW_VECS; ++v)
+            for (int v = 0; v < G::VECS; ++v)
                 xv[v] = make_uint4(0u, 0u, 0u, 0u);
         }
         if (patched) {
-            // A operand: my U row split into bf16 hi / lo (zeros for an empty row)
-            float u[KP];
-            if (src >= 0) {
-                load_factor_row(p.patch.u[ch] + (int64_t)l * p.patch.u_ls[ch] +
-                                    (t0 + i) * p.patch.u_ts[ch],
-                                m, u);
-            } else {
+            // A operand: the tile's U rows split into bf16 hi / lo; each row is
+            // converted by its column groups, 16 / GROUPS ranks each
 #pragma unroll
-                for (int r = 0; r < KP; ++r)
-                    u[r] = 0.0f;
+            for (int k0 = grp * (KP / G::GROUPS); k0 < (grp + 1) * (KP / G::GROUPS); k0 += 8) {
+                float u[8];
+                if (src >= 0) {
+                    load_factor8(p.patch.u[ch] + (int64_t)l * p.patch.u_ls[ch] +
+                                     (t0 + i) * p.patch.u_ts[ch],
+                                 k0, m, u);
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+                        u[r] = 0.0f;
+                }
+                split_store8(u, a_hi + kmajor_off(row, k0), a_lo + kmajor_off(row, k0));
             }
-            split_store8(u, a_hi + kmajor_off(tid, 0), a_lo + kmajor_off(tid, 0));
-            split_store8(u + 8, a_hi + kmajor_off(tid, 8), a_lo + kmajor_off(tid, 8));
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             fence_before();
             __syncthreads(); // A complete; the previous tile's accumulator reads are done
             if (tid == 0) {
                 fence_after();
-                mma_bf16(tmem, smem_desc(a_hi), smem_desc(b_hi), 0u);
-                mma_bf16(tmem, smem_desc(a_hi), smem_desc(b_lo), 1u);
-                mma_bf16(tmem, smem_desc(a_lo), smem_desc(b_hi), 1u);
+                mma_bf16<G::NB>(tmem, smem_desc(a_hi), smem_desc(b_hi), 0u);
+                mma_bf16<G::NB>(tmem, smem_desc(a_hi), smem_desc(b_lo), 1u);
+                mma_bf16<G::NB>(tmem, smem_desc(a_lo), smem_desc(b_hi), 1u);
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                              : "memory");
                 if (!mbar_wait(bar, phase, MMA_WAIT_NS)) {
@@ -276,28 +305,50 @@ __global__ void __launch_bounds__(NT, 4) patch_tc_kernel(const __grid_constant__
             if (!s_ok)
                 break;
         }
-        // my output row, 16 columns (or 16 rotary pairs) at a time
+        // my output columns, 16 (or 16 rotary pairs) at a time
         const uint32_t *xw = reinterpret_cast<const uint32_t *>(xv);
         uint4 *dp = reinterpret_cast<uint4 *>(dst_base + (dst >= 0 ? dst : 0) * dst_ss);
+        if (!patched) {
+            // this channel carries no patch: verbatim copy, or the correctly
+            // rounded rotation of the unpatched relocation
+            if (dst < 0)
+                continue;
+            if (!rotate) {
+#pragma unroll
+                for (int v = 0; v < G::VECS; ++v)
+                    __stcs(dp + v, xv[v]);
+                continue;
+            }
+#pragma unroll
+            for (int f0 = 0; f0 < G::HALF; f0 += 8) {
+                uint32_t o1[4], o2[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const uint32_t w1 = xw[(f0 + e) >> 1], w2 = xw[(f0 + G::HALF + e) >> 1];
+                    const float4 q0 = cs_s[f0 + e], q1 = cs_s[f0 + e + 1];
+                    o1[e >> 1] = rotate_one(w1 & 0xFFFFu, w2 & 0xFFFFu, q0, true, 0.0f) |
+                                 (rotate_one(w1 >> 16, w2 >> 16, q1, true, 0.0f) << 16);
+                    o2[e >> 1] = rotate_one(w1 & 0xFFFFu, w2 & 0xFFFFu, q0, false, 0.0f) |
+                                 (rotate_one(w1 >> 16, w2 >> 16, q1, false, 0.0f) << 16);
+                }
+                __stcs(dp + f0 / 8, make_uint4(o1[0], o1[1], o1[2], o1[3]));
+                __stcs(dp + (f0 + G::HALF) / 8, make_uint4(o2[0], o2[1], o2[2], o2[3]));
+            }
+            continue;
+        }
         if (rotate) {
 #pragma unroll
-            for (int f0 = 0; f0 < HALF; f0 += 16) {
+            for (int f0 = 0; f0 < G::HALF; f0 += 16) {
                 uint32_t a1[16], a2[16];
-                if (patched) {
-                    tmem_ld16(t_row + (uint32_t)f0, a1);
-                    tmem_ld16(t_row + (uint32_t)(f0 + HALF), a2);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        a1[e] = a2[e] = 0u;
-                }
+                tmem_ld16(t_row + (uint32_t)f0, a1);
+                tmem_ld16(t_row + (uint32_t)(f0 + G::HALF), a2);
                 uint32_t o1[8], o2[8];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    // (x1, x2) = (x[j], x[j+64]) turned by δθ_j; cos = c1 + c2,
+                    // (x1, x2) = (x[j], x[j+D/2]) turned by δθ_j; cos = c1 + c2,
                     // sin = s1 + s2 with c1, s1 short enough for exact products
                     const float4 q = cs_s[f0 + e];
-                    const uint32_t w1 = xw[(f0 + e) >> 1], w2 = xw[(f0 + HALF + e) >> 1];
+                    const uint32_t w1 = xw[(f0 + e) >> 1], w2 = xw[(f0 + G::HALF + e) >> 1];
                     const float x1 = (e & 1) ? bf16_hi(w1) : bf16_lo(w1);
                     const float x2 = (e & 1) ? bf16_hi(w2) : bf16_lo(w2);
                     const float r1 = fmaf(x1, q.x, -(x2 * q.z)) +
@@ -316,21 +367,15 @@ __global__ void __launch_bounds__(NT, 4) patch_tc_kernel(const __grid_constant__
                 if (dst >= 0) {
                     __stcs(dp + f0 / 8, make_uint4(o1[0], o1[1], o1[2], o1[3]));
                     __stcs(dp + f0 / 8 + 1, make_uint4(o1[4], o1[5], o1[6], o1[7]));
-                    __stcs(dp + (f0 + HALF) / 8, make_uint4(o2[0], o2[1], o2[2], o2[3]));
-                    __stcs(dp + (f0 + HALF) / 8 + 1, make_uint4(o2[4], o2[5], o2[6], o2[7]));
+                    __stcs(dp + (f0 + G::HALF) / 8, make_uint4(o2[0], o2[1], o2[2], o2[3]));
+                    __stcs(dp + (f0 + G::HALF) / 8 + 1, make_uint4(o2[4], o2[5], o2[6], o2[7]));
                 }
             }
         } else {
 #pragma unroll
-            for (int c16 = 0; c16 < NB; c16 += 16) {
+            for (int c16 = 0; c16 < G::W; c16 += 16) {
                 uint32_t a[16];
-                if (patched) {
-                    tmem_ld16(t_row + (uint32_t)c16, a);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        a[e] = 0u;
-                }
+                tmem_ld16(t_row + (uint32_t)c16, a);
                 uint32_t o[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -349,30 +394,47 @@ __global__ void __launch_bounds__(NT, 4) patch_tc_kernel(const __grid_constant__
     __syncthreads();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(TMEM_COLS)
+                     "r"((uint32_t)G::NB)
                      : "memory");
+}
+
+template <class G>
+static cudaError_t launch_geo(const RelocParams &p, TcLaunch tl, cudaStream_t stream)
+{
+    const int64_t blocks = (int64_t)p.num_chunks * tl.nch * tl.slices;
+    if (blocks == 0)
+        return cudaSuccess;
+    if (blocks > 0x7FFFFFFFll)
+        return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)blocks, (unsigned)p.src.num_layers);
+    if (p.in_place)
+        patch_tc_kernel<G, false><<<grid, G::NT, 0, stream>>>(p, tl);
+    else
+        patch_tc_kernel<G, true><<<grid, G::NT, 0, stream>>>(p, tl);
+    return cudaGetLastError();
 }
 
 } // namespace tc
 
 bool patch_tc_supported(const RelocParams &p, RowKind kind)
 {
-    return kind == RowKind::Gqa && p.patched && p.patch.m <= tc::KP &&
-           p.src.num_layers <= 65535;
+    (void)kind;
+    return p.patched && p.patch.m <= tc::KP && p.src.num_layers <= 65535;
 }
 
-cudaError_t launch_patch_tc(const RelocParams &p, cudaStream_t stream)
+int patch_tc_launches(RowKind kind) { return kind == RowKind::Gqa ? 1 : 2; }
+
+cudaError_t launch_patch_tc(const RelocParams &p, RowKind kind, cudaStream_t stream)
 {
     if (p.num_chunks == 0)
         return cudaSuccess;
-    if ((int64_t)p.num_chunks * 2 * tc::SLICES > 0x7FFFFFFFll)
-        return cudaErrorInvalidConfiguration;
-    const dim3 grid((unsigned)(p.num_chunks * 2 * tc::SLICES), (unsigned)p.src.num_layers);
-    if (p.in_place)
-        tc::patch_tc_kernel<false><<<grid, tc::NT, 0, stream>>>(p);
-    else
-        tc::patch_tc_kernel<true><<<grid, tc::NT, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (kind == RowKind::Gqa) // both channels 1024 wide: 4 slices of two heads
+        return tc::launch_geo<tc::TcGeo<256, 128>>(p, tc::TcLaunch{0, 2, 4}, stream);
+    // MLA: the 512-wide latent as 2 slices of 256, the 64-wide k_pe as one slice
+    cudaError_t e = tc::launch_geo<tc::TcGeo<256, 128>>(p, tc::TcLaunch{0, 1, 2}, stream);
+    if (e != cudaSuccess)
+        return e;
+    return tc::launch_geo<tc::TcGeo<64, 64>>(p, tc::TcLaunch{1, 1, 1}, stream);
 }
 
 } // namespace kvr

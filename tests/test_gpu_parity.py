@@ -148,11 +148,35 @@ def test_standalone_patch(orc, shape):
                 dev["chunk_dst_pos"], dev["block_tables"], wl.block_tables.shape[0],
                 wl.block_tables.shape[1], pd, ws)
     assert kv.kv_get_device_status(ws) == kv.KV_OK
-    assert kv.kv_last_launch_count() == 1
+    # one kernel per distinct channel width: MLA rows are 512 + 64 wide, GQA 1024 + 1024
+    assert kv.kv_last_launch_count() == (2 if shape == "mla" else 1)
     assert orc.patch_apply(dst.orc, wl.tok_off, wl.chunk_req, wl.chunk_dst_pos, wl.block_tables,
                            O.Patch(m, [x.numpy() for x in us],
                                    [x.numpy() for x in vs])) == O.OK
     check_pool(dst, f"patch {shape}", copy_exact=False)
+
+
+@pytest.mark.parametrize("shape", ["mla", "gqa"])
+@pytest.mark.parametrize("patched_ch", [0, 1])
+def test_patch_on_one_channel_only(orc, shape, patched_ch):
+    # the other channel is copied verbatim / rotated exactly, as without a patch
+    wl, src, dst, dev = _reloc_case(shape, 245 + patched_ch, num_reqs=2, chunks=3,
+                                    deltas=[0, 3, -20000])
+    m = 4  # ranks are multiples of 4
+    widths = (src.cd, src.H * src.d)
+    us, vs = [None, None], [None, None]
+    us[patched_ch] = synth.f32_normal((L, wl.total_tokens, m), 247, std=0.03)
+    vs[patched_ch] = synth.f32_normal((L, wl.num_chunks, widths[patched_ch], m), 248,
+                                      std=0.03)
+    pd = kv.patch_desc(m, [None if x is None else x.cuda() for x in us],
+                       [None if x is None else x.cuda() for x in vs])
+    assert _run_relocate(wl, src, dst, dev, patch=pd) == kv.KV_OK
+    _oracle_relocate(orc, wl, src, dst, O.Patch(m, [None if x is None else x.numpy() for x in us],
+                                                [None if x is None else x.numpy() for x in vs]))
+    stats = check_pool(dst, f"one-channel patch {shape} ch{patched_ch}",
+                       copy_exact=patched_ch == 1)
+    if patched_ch == 0:  # the unpatched rotation keeps the oracle's bits, as without a patch
+        assert stats["exact"] >= stats["values"] - max(3, stats["values"] // 100000), stats
 
 
 def test_relocate_reports_a_bad_index_and_skips_its_row(orc):

@@ -5,23 +5,23 @@
 // channel) the patch is the product of U (rows x m) and V (cols x m)ᵀ, a
 // dense contraction with a short inner dimension (m <= 16).  A block owns a
 // slice of NB columns of one channel of one (chunk, layer) and walks the
-// chunk in tiles of 128 rows.  Its threads are (row, column group): row =
-// tensor-memory lane, a group of W columns (one rotary head, W = D, for the
-// rotated channel), so a thread holds both halves of every rotary pair it
-// writes.  Per tile:
-//   * each thread loads its row's W columns into registers (they fly while
-//     the patch is being formed) and converts its share of the tile's U rows
-//     into bf16 high and low parts (x ~ hi + lo to ~16 bits), stored as
-//     K-major core matrices (8 rows x 16 B) -- once per slice, shared by all
-//     its heads;
-//   * V's slice was split the same way once per block; three tcgen05.mma
-//     kind::f16 (hi·hi, hi·lo, lo·hi) accumulate the 128 x NB fp32 product in
-//     tensor memory;
-//   * each thread reads its part of the product 16 columns at a time with
-//     tcgen05.ld, forms rnd(R(δ)·x + patch) (rotated channel) or
-//     rnd(x + patch) and stores it with 16-byte writes.
-// The wait for the MMAs is a bounded poll of an mbarrier; tensor memory is
-// released on every path.
+// chunk in tiles of 128 rows.  Per tile:
+//   * threads 0..127 each gather one row of the slice (NB x 2 bytes at its
+//     source slot) into shared memory with a bulk copy (the TMA engine), so
+//     the rows fly without occupying the load/store units;
+//   * meanwhile the block converts the tile's U rows into bf16 high and low
+//     parts (x ~ hi + lo to ~16 bits), stored as K-major core matrices
+//     (8 rows x 16 B) once per slice; V's slice was split the same way once
+//     per block; three tcgen05.mma kind::f16 (hi·hi, hi·lo, lo·hi)
+//     accumulate the 128 x NB fp32 product in tensor memory;
+//   * each thread is (row = tensor-memory lane, group of W columns = one
+//     rotary head for the rotated channel, W = D), so it holds both halves
+//     of every rotary pair it rewrites: it reads its part of the product 16
+//     columns at a time with tcgen05.ld, forms rnd(R(δ)·x + patch) (rotated
+//     channel) or rnd(x + patch) and writes it back into the tile;
+//   * threads 0..127 write the rows to their target slots with bulk copies.
+// The waits for copies and MMAs are bounded polls of mbarriers; tensor
+// memory is released on every path.
 #include <cuda_bf16.h>
 
 #include "kv_launch.h"
@@ -154,20 +154,72 @@ __device__ __forceinline__ void load_factor8(const float *row, int k0, int m, fl
     }
 }
 
+// Bulk (non-tensor) TMA copies of whole rows between global and shared
+// memory; addresses and sizes are multiples of 16 bytes.
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, uint32_t bytes,
+                                          uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gmem_src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(void *gmem_dst, const void *smem_src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+                 "r"((uint32_t)__cvta_generic_to_shared(smem_src)), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
 // Which blocks a launch covers: channels [ch0, ch0 + nch), `slices` slices
 // of NB columns each; block x = (chunk * nch + ch - ch0) * slices + slice.
 struct TcLaunch {
     int32_t ch0, nch, slices;
 };
 
+// Dynamic shared memory of one block: A (hi, lo), B (hi, lo), then the row
+// tile, M rows of PITCH bytes.  The 16 spare bytes per row shift consecutive
+// rows by four banks, so a warp reading the same piece of 32 rows is free of
+// bank conflicts.
+template <class G>
+struct TcSmem {
+    static constexpr int ROW_BYTES = G::NB * 2;
+    static constexpr int PITCH = ROW_BYTES + 16;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = 2 * A_BYTES;
+    static constexpr int X_OFF = B_OFF + 2 * G::B_BYTES;
+    static constexpr int BYTES = X_OFF + M * PITCH;
+};
+
+// A block owns NB columns of one channel of one (chunk, layer).  Per tile of
+// 128 rows: threads 0..127 each gather one row with a bulk copy into shared
+// memory while the block forms the A operand and the MMAs run; then every
+// thread rewrites its (row, column group) of the tile in shared memory and
+// threads 0..127 write the rows back with bulk copies.
 template <class G, bool RELOC>
 __global__ void __launch_bounds__(G::NT, G::MIN_BLOCKS)
 patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
 {
-    __shared__ __align__(128) unsigned char a_hi[A_BYTES], a_lo[A_BYTES];
-    __shared__ __align__(128) unsigned char b_hi[G::B_BYTES], b_lo[G::B_BYTES];
-    __shared__ float4 cs_s[G::HALF > 0 ? G::HALF : 1]; // (c1, c2, s1, s2) per frequency
-    __shared__ __align__(8) uint64_t s_mbar;
+    using S = TcSmem<G>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char *a_hi = smem + S::A_OFF, *a_lo = a_hi + A_BYTES;
+    unsigned char *b_hi = smem + S::B_OFF, *b_lo = b_hi + G::B_BYTES;
+    unsigned char *xs = smem + S::X_OFF;
+    __shared__ float4 cs_s[G::HALF]; // (c1, c2, s1, s2) per frequency
+    __shared__ __align__(8) uint64_t s_bar[2]; // [0] rows landed, [1] MMAs done
     __shared__ uint32_t s_tmem;
     __shared__ int32_t s_ok;
 
@@ -180,6 +232,9 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
         if (p.tok_off[0] != 0 || p.tok_off[p.num_chunks] != p.total_tokens)
             set_status(p.status, kStatusOutOfRange);
     }
+    const bool patched = p.patch.u[ch] != nullptr;
+    if (!RELOC && !patched)
+        return; // in place and nothing to add: the rows stay as they are
     const int64_t t0 = p.tok_off[c];
     const int64_t n = max((int64_t)0, (int64_t)p.tok_off[c + 1] - t0);
     const int32_t req = p.chunk_req[c];
@@ -187,22 +242,20 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
     const int32_t *bt = p.block_tables + (int64_t)(req_ok ? req : 0) * p.max_blocks;
     const int64_t pos0 = p.chunk_dst_pos[c];
     const bool rotate = RELOC && ch == 1 && p.delta[c] != 0;
-    const bool patched = p.patch.u[ch] != nullptr;
-    if (!RELOC && !patched)
-        return; // in place and nothing to add: the rows stay as they are
     const int m = p.patch.m;
-    const int row = (warp & 3) * 32 + lane; // my row of the tile = TMEM lane
+    const bool owner = tid < M;             // gathers / writes back row `tid`
+    const int row = (warp & 3) * 32 + lane; // my row in the rewrite = TMEM lane
     const int grp = warp >> 2;              // my column group
-    const int cg = grp * G::W;              // its first column in the slice
+    const int cg = grp * G::W;
     const PoolView &sp = RELOC ? p.src : p.dst;
     const char *src_base = (ch == 0 ? sp.copy + (int64_t)l * sp.copy_ls
-                                    : sp.rot + (int64_t)l * sp.rot_ls) + (col0 + cg) * 2;
+                                    : sp.rot + (int64_t)l * sp.rot_ls) + col0 * 2;
     const int64_t src_ss = ch == 0 ? sp.copy_ss : sp.rot_ss;
     char *dst_base = (ch == 0 ? p.dst.copy + (int64_t)l * p.dst.copy_ls
-                              : p.dst.rot + (int64_t)l * p.dst.rot_ls) + (col0 + cg) * 2;
+                              : p.dst.rot + (int64_t)l * p.dst.rot_ls) + col0 * 2;
     const int64_t dst_ss = ch == 0 ? p.dst.copy_ss : p.dst.rot_ss;
 
-    // --- once per block: V's slice as the B operand, cos/sin, barrier, TMEM
+    // --- once per block: V's slice as the B operand, cos/sin, barriers, TMEM
     if (patched) {
         const float *vb = p.patch.v[ch] + (int64_t)l * p.patch.v_ls[ch] +
                           (int64_t)c * p.patch.v_cs[ch] + (int64_t)col0 * p.patch.v_cols[ch];
@@ -215,12 +268,15 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
     }
     if (rotate && tid < G::HALF)
         cs_s[tid] = p.table[(int64_t)c * G::HALF + tid];
-    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&s_mbar);
+    const uint32_t bar_x = (uint32_t)__cvta_generic_to_shared(&s_bar[0]);
+    const uint32_t bar_mma = (uint32_t)__cvta_generic_to_shared(&s_bar[1]);
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar_x), "r"(M) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_mma) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_ok = 1;
     }
-    if (warp == 0) {
+    if (patched && warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          (uint32_t)__cvta_generic_to_shared(&s_tmem)),
                      "r"((uint32_t)G::NB)
@@ -230,57 +286,69 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
     fence_before();
     __syncthreads();
     fence_after();
-    const uint32_t tmem = s_tmem;
+    const uint32_t tmem = patched ? s_tmem : 0u;
     const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)cg;
 
-    const int64_t ntiles = (n + M - 1) / M;
-    uint32_t phase = 0;
-    for (int64_t t = 0; t < ntiles; ++t) {
-        // my row: slots, then its W columns start flying into registers
-        const int64_t i = t * M + row;
-        int64_t src = -1, dst = -1;
-        if (i < n) {
-            if (req_ok)
-                dst = slot_of(bt, p.max_blocks, p.dst.block, p.dst.num_blocks, pos0 + i);
-            if (RELOC) {
-                const int64_t sl = p.src_slots[t0 + i];
-                src = (sl >= 0 && sl < p.src.num_slots) ? sl : -1;
-            } else {
-                src = dst;
-            }
-            if (src < 0 || dst < 0) {
-                if (grp == 0)
-                    set_status(p.status, kStatusOutOfRange);
-                src = dst = -1;
-            }
-        }
-        uint4 xv[G::VECS];
-        if (src >= 0) {
-            const uint4 *xs = reinterpret_cast<const uint4 *>(src_base + src * src_ss);
-#pragma unroll
-            for (int v = 0; v < G::VECS; ++v)
-                xv[v] = xs[v];
+    // slots of row `tid` of tile t (owners only); a bad index is reported and
+    // its row skipped
+    auto row_slots = [&](int64_t t, int64_t &src, int64_t &dst) {
+        const int64_t i = t * M + tid;
+        src = dst = -1;
+        if (i >= n)
+            return;
+        if (req_ok)
+            dst = slot_of(bt, p.max_blocks, p.dst.block, p.dst.num_blocks, pos0 + i);
+        if (RELOC) {
+            const int64_t sl = p.src_slots[t0 + i];
+            src = (sl >= 0 && sl < p.src.num_slots) ? sl : -1;
         } else {
-#pragma unroll
-            for (int v = 0; v < G::VECS; ++v)
-                xv[v] = make_uint4(0u, 0u, 0u, 0u);
+            src = dst;
+        }
+        if (src < 0 || dst < 0) {
+            set_status(p.status, kStatusOutOfRange);
+            src = dst = -1;
+        }
+    };
+
+    const int64_t ntiles = (n + M - 1) / M;
+    unsigned char *my_row = xs + tid * S::PITCH;                   // owner's row
+    unsigned char *xr = xs + row * S::PITCH + cg * 2;              // my part in the rewrite
+    uint4 *xq = reinterpret_cast<uint4 *>(xr);
+    int64_t src = -1, dst = -1;
+    if (owner && ntiles > 0)
+        row_slots(0, src, dst);
+    uint32_t ph_x = 0, ph_mma = 0;
+    for (int64_t t = 0; t < ntiles; ++t) {
+        int64_t my_dst = -1;
+        if (owner) {
+            // the previous tile's write-back has finished reading this row
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            if (src >= 0) {
+                mbar_arrive_tx(bar_x, S::ROW_BYTES);
+                bulk_load(my_row, src_base + src * src_ss, S::ROW_BYTES, bar_x);
+            } else {
+                mbar_arrive(bar_x);
+            }
+            my_dst = dst;
+            if (t + 1 < ntiles) // the next tile's slots, while this one is in flight
+                row_slots(t + 1, src, dst);
         }
         if (patched) {
-            // A operand: the tile's U rows split into bf16 hi / lo; each row is
-            // converted by its column groups, 16 / GROUPS ranks each
-#pragma unroll
-            for (int k0 = grp * (KP / G::GROUPS); k0 < (grp + 1) * (KP / G::GROUPS); k0 += 8) {
+            // A operand: the tile's U rows split into bf16 hi / lo (zero past the chunk)
+            for (int e = tid; e < M * 2; e += G::NT) {
+                const int r = e >> 1, k0 = (e & 1) * 8;
+                const int64_t i = t * M + r;
                 float u[8];
-                if (src >= 0) {
+                if (i < n) {
                     load_factor8(p.patch.u[ch] + (int64_t)l * p.patch.u_ls[ch] +
                                      (t0 + i) * p.patch.u_ts[ch],
                                  k0, m, u);
                 } else {
 #pragma unroll
-                    for (int r = 0; r < 8; ++r)
-                        u[r] = 0.0f;
+                    for (int q = 0; q < 8; ++q)
+                        u[q] = 0.0f;
                 }
-                split_store8(u, a_hi + kmajor_off(row, k0), a_lo + kmajor_off(row, k0));
+                split_store8(u, a_hi + kmajor_off(r, k0), a_lo + kmajor_off(r, k0));
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             fence_before();
@@ -290,65 +358,45 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
                 mma_bf16<G::NB>(tmem, smem_desc(a_hi), smem_desc(b_hi), 0u);
                 mma_bf16<G::NB>(tmem, smem_desc(a_hi), smem_desc(b_lo), 1u);
                 mma_bf16<G::NB>(tmem, smem_desc(a_lo), smem_desc(b_hi), 1u);
-                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_mma)
                              : "memory");
-                if (!mbar_wait(bar, phase, MMA_WAIT_NS)) {
+                if (!mbar_wait(bar_mma, ph_mma, MMA_WAIT_NS)) {
                     set_status(p.status, kStatusTimeout);
-                    // give the MMAs one more bounded wait before the memory is released
-                    mbar_wait(bar, phase, MMA_WAIT_NS);
+                    mbar_wait(bar_mma, ph_mma, MMA_WAIT_NS); // once more before memory is released
                     s_ok = 0;
                 }
             }
-            phase ^= 1u;
-            __syncthreads();
-            fence_after();
-            if (!s_ok)
-                break;
+            ph_mma ^= 1u;
         }
-        // my output columns, 16 (or 16 rotary pairs) at a time
-        const uint32_t *xw = reinterpret_cast<const uint32_t *>(xv);
-        uint4 *dp = reinterpret_cast<uint4 *>(dst_base + (dst >= 0 ? dst : 0) * dst_ss);
-        if (!patched) {
-            // this channel carries no patch: verbatim copy, or the correctly
-            // rounded rotation of the unpatched relocation
-            if (dst < 0)
-                continue;
-            if (!rotate) {
-#pragma unroll
-                for (int v = 0; v < G::VECS; ++v)
-                    __stcs(dp + v, xv[v]);
-                continue;
-            }
-#pragma unroll
-            for (int f0 = 0; f0 < G::HALF; f0 += 8) {
-                uint32_t o1[4], o2[4];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const uint32_t w1 = xw[(f0 + e) >> 1], w2 = xw[(f0 + G::HALF + e) >> 1];
-                    const float4 q0 = cs_s[f0 + e], q1 = cs_s[f0 + e + 1];
-                    o1[e >> 1] = rotate_one(w1 & 0xFFFFu, w2 & 0xFFFFu, q0, true, 0.0f) |
-                                 (rotate_one(w1 >> 16, w2 >> 16, q1, true, 0.0f) << 16);
-                    o2[e >> 1] = rotate_one(w1 & 0xFFFFu, w2 & 0xFFFFu, q0, false, 0.0f) |
-                                 (rotate_one(w1 >> 16, w2 >> 16, q1, false, 0.0f) << 16);
-                }
-                __stcs(dp + f0 / 8, make_uint4(o1[0], o1[1], o1[2], o1[3]));
-                __stcs(dp + (f0 + G::HALF) / 8, make_uint4(o2[0], o2[1], o2[2], o2[3]));
-            }
-            continue;
+        if (!mbar_wait(bar_x, ph_x, MMA_WAIT_NS)) {
+            set_status(p.status, kStatusTimeout);
+            mbar_wait(bar_x, ph_x, MMA_WAIT_NS); // the copies in flight, once more
+            s_ok = 0;
         }
-        if (rotate) {
+        ph_x ^= 1u;
+        __syncthreads();
+        fence_after();
+        if (!s_ok)
+            break;
+
+        // rewrite my (row, column group) of the tile in place
+        if (patched && rotate) {
 #pragma unroll
             for (int f0 = 0; f0 < G::HALF; f0 += 16) {
                 uint32_t a1[16], a2[16];
                 tmem_ld16(t_row + (uint32_t)f0, a1);
                 tmem_ld16(t_row + (uint32_t)(f0 + G::HALF), a2);
+                const uint4 p0 = xq[f0 / 8], p1 = xq[f0 / 8 + 1];
+                const uint4 q0 = xq[(f0 + G::HALF) / 8], q1 = xq[(f0 + G::HALF) / 8 + 1];
+                const uint32_t w1s[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                const uint32_t w2s[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                 uint32_t o1[8], o2[8];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     // (x1, x2) = (x[j], x[j+D/2]) turned by δθ_j; cos = c1 + c2,
                     // sin = s1 + s2 with c1, s1 short enough for exact products
                     const float4 q = cs_s[f0 + e];
-                    const uint32_t w1 = xw[(f0 + e) >> 1], w2 = xw[(f0 + G::HALF + e) >> 1];
+                    const uint32_t w1 = w1s[e >> 1], w2 = w2s[e >> 1];
                     const float x1 = (e & 1) ? bf16_hi(w1) : bf16_lo(w1);
                     const float x2 = (e & 1) ? bf16_hi(w2) : bf16_lo(w2);
                     const float r1 = fmaf(x1, q.x, -(x2 * q.z)) +
@@ -364,35 +412,60 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
                         o2[e >> 1] = b2;
                     }
                 }
-                if (dst >= 0) {
-                    __stcs(dp + f0 / 8, make_uint4(o1[0], o1[1], o1[2], o1[3]));
-                    __stcs(dp + f0 / 8 + 1, make_uint4(o1[4], o1[5], o1[6], o1[7]));
-                    __stcs(dp + (f0 + G::HALF) / 8, make_uint4(o2[0], o2[1], o2[2], o2[3]));
-                    __stcs(dp + (f0 + G::HALF) / 8 + 1, make_uint4(o2[4], o2[5], o2[6], o2[7]));
-                }
+                xq[f0 / 8] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                xq[f0 / 8 + 1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+                xq[(f0 + G::HALF) / 8] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                xq[(f0 + G::HALF) / 8 + 1] = make_uint4(o2[4], o2[5], o2[6], o2[7]);
             }
-        } else {
+        } else if (patched) {
 #pragma unroll
             for (int c16 = 0; c16 < G::W; c16 += 16) {
                 uint32_t a[16];
                 tmem_ld16(t_row + (uint32_t)c16, a);
+                const uint4 p0 = xq[c16 / 8], p1 = xq[c16 / 8 + 1];
+                const uint32_t ws[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
                 uint32_t o[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t w = xw[c16 / 2 + e];
-                    o[e] = bf16_rne(bf16_lo(w) + __uint_as_float(a[2 * e])) |
-                           (bf16_rne(bf16_hi(w) + __uint_as_float(a[2 * e + 1])) << 16);
+                for (int e = 0; e < 8; ++e)
+                    o[e] = bf16_rne(bf16_lo(ws[e]) + __uint_as_float(a[2 * e])) |
+                           (bf16_rne(bf16_hi(ws[e]) + __uint_as_float(a[2 * e + 1])) << 16);
+                xq[c16 / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+                xq[c16 / 8 + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+        } else if (rotate) {
+            // no factors on this channel: the correctly rounded rotation of
+            // the unpatched relocation (the verbatim part needs no rewrite)
+#pragma unroll
+            for (int f0 = 0; f0 < G::HALF; f0 += 8) {
+                const uint4 pa = xq[f0 / 8], pb = xq[(f0 + G::HALF) / 8];
+                const uint32_t w1s[4] = {pa.x, pa.y, pa.z, pa.w};
+                const uint32_t w2s[4] = {pb.x, pb.y, pb.z, pb.w};
+                uint32_t o1[4], o2[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t w1 = w1s[e], w2 = w2s[e];
+                    const float4 c0 = cs_s[f0 + 2 * e], c1 = cs_s[f0 + 2 * e + 1];
+                    o1[e] = rotate_one(w1 & 0xFFFFu, w2 & 0xFFFFu, c0, true, 0.0f) |
+                            (rotate_one(w1 >> 16, w2 >> 16, c1, true, 0.0f) << 16);
+                    o2[e] = rotate_one(w1 & 0xFFFFu, w2 & 0xFFFFu, c0, false, 0.0f) |
+                            (rotate_one(w1 >> 16, w2 >> 16, c1, false, 0.0f) << 16);
                 }
-                if (dst >= 0) {
-                    __stcs(dp + c16 / 8, make_uint4(o[0], o[1], o[2], o[3]));
-                    __stcs(dp + c16 / 8 + 1, make_uint4(o[4], o[5], o[6], o[7]));
-                }
+                xq[f0 / 8] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                xq[(f0 + G::HALF) / 8] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
             }
         }
+        // generic-proxy writes of the tile become visible to the bulk copies
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        fence_before();
+        __syncthreads();
+        if (owner && my_dst >= 0)
+            bulk_store(dst_base + my_dst * dst_ss, my_row, S::ROW_BYTES);
     }
+    if (owner)
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     fence_before();
     __syncthreads();
-    if (warp == 0)
+    if (patched && warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"((uint32_t)G::NB)
                      : "memory");
@@ -407,10 +480,19 @@ static cudaError_t launch_geo(const RelocParams &p, TcLaunch tl, cudaStream_t st
     if (blocks > 0x7FFFFFFFll)
         return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)blocks, (unsigned)p.src.num_layers);
-    if (p.in_place)
-        patch_tc_kernel<G, false><<<grid, G::NT, 0, stream>>>(p, tl);
-    else
-        patch_tc_kernel<G, true><<<grid, G::NT, 0, stream>>>(p, tl);
+    constexpr int smem = TcSmem<G>::BYTES;
+    cudaError_t e;
+    if (p.in_place) {
+        if ((e = cudaFuncSetAttribute(patch_tc_kernel<G, false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+            return e;
+        patch_tc_kernel<G, false><<<grid, G::NT, smem, stream>>>(p, tl);
+    } else {
+        if ((e = cudaFuncSetAttribute(patch_tc_kernel<G, true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+            return e;
+        patch_tc_kernel<G, true><<<grid, G::NT, smem, stream>>>(p, tl);
+    }
     return cudaGetLastError();
 }
 

@@ -154,6 +154,63 @@ __device__ __forceinline__ void load_factor8(const float *row, int k0, int m, fl
     }
 }
 
+// Two fp32 lanes in one 64-bit register, for the packed f32x2 arithmetic.
+typedef unsigned long long f2;
+
+// bf16 pair (low half = first element) -> fp32 pair, exact.
+__device__ __forceinline__ f2 f2_of_bf16x2(uint32_t w)
+{
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+    return r;
+}
+
+__device__ __forceinline__ f2 f2_of_bits(uint32_t lo, uint32_t hi)
+{
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c)
+{
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b)
+{
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b)
+{
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// fp32 pair -> bf16 pair, each rounded to nearest even (NaN stays NaN).
+__device__ __forceinline__ uint32_t bf16x2_rne(f2 v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// True when either lane is NaN.
+__device__ __forceinline__ bool f2_has_nan(f2 v)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+    return lo != lo || hi != hi;
+}
+
 // Bulk (non-tensor) TMA copies of whole rows between global and shared
 // memory; addresses and sizes are multiples of 16 bytes.
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes)
@@ -218,7 +275,9 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
     unsigned char *a_hi = smem + S::A_OFF, *a_lo = a_hi + A_BYTES;
     unsigned char *b_hi = smem + S::B_OFF, *b_lo = b_hi + G::B_BYTES;
     unsigned char *xs = smem + S::X_OFF;
-    __shared__ float4 cs_s[G::HALF]; // (c1, c2, s1, s2) per frequency
+    // cos/sin per pair of frequencies k = (2k, 2k+1): cs_c[k] = (c1, c1', c2, c2'),
+    // cs_s[k] = (s1, s1', s2, s2'); cos = c1 + c2, sin = s1 + s2
+    __shared__ __align__(16) float cs_c[G::HALF * 2], cs_s[G::HALF * 2];
     __shared__ __align__(8) uint64_t s_bar[2]; // [0] rows landed, [1] MMAs done
     __shared__ uint32_t s_tmem;
     __shared__ int32_t s_ok;
@@ -266,8 +325,14 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
             split_store8(v, b_hi + kmajor_off(nn, k0), b_lo + kmajor_off(nn, k0));
         }
     }
-    if (rotate && tid < G::HALF)
-        cs_s[tid] = p.table[(int64_t)c * G::HALF + tid];
+    if (rotate && tid < G::HALF) {
+        const float4 q = p.table[(int64_t)c * G::HALF + tid];
+        const int at = (tid >> 1) * 4 + (tid & 1);
+        cs_c[at] = q.x;
+        cs_c[at + 2] = q.y;
+        cs_s[at] = q.z;
+        cs_s[at + 2] = q.w;
+    }
     const uint32_t bar_x = (uint32_t)__cvta_generic_to_shared(&s_bar[0]);
     const uint32_t bar_mma = (uint32_t)__cvta_generic_to_shared(&s_bar[1]);
     if (tid == 0) {
@@ -381,6 +446,8 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
 
         // rewrite my (row, column group) of the tile in place
         if (patched && rotate) {
+            const ulonglong2 *cc = reinterpret_cast<const ulonglong2 *>(cs_c);
+            const ulonglong2 *ss = reinterpret_cast<const ulonglong2 *>(cs_s);
 #pragma unroll
             for (int f0 = 0; f0 < G::HALF; f0 += 16) {
                 uint32_t a1[16], a2[16];
@@ -391,25 +458,47 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
                 const uint32_t w1s[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
                 const uint32_t w2s[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
                 uint32_t o1[8], o2[8];
+                f2 chk = 0ull;
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    // (x1, x2) = (x[j], x[j+D/2]) turned by δθ_j; cos = c1 + c2,
-                    // sin = s1 + s2 with c1, s1 short enough for exact products
-                    const float4 q = cs_s[f0 + e];
-                    const uint32_t w1 = w1s[e >> 1], w2 = w2s[e >> 1];
-                    const float x1 = (e & 1) ? bf16_hi(w1) : bf16_lo(w1);
-                    const float x2 = (e & 1) ? bf16_hi(w2) : bf16_lo(w2);
-                    const float r1 = fmaf(x1, q.x, -(x2 * q.z)) +
-                                     (fmaf(x1, q.y, -(x2 * q.w)) + __uint_as_float(a1[e]));
-                    const float r2 = fmaf(x2, q.x, x1 * q.z) +
-                                     (fmaf(x2, q.y, x1 * q.w) + __uint_as_float(a2[e]));
-                    const uint32_t b1 = bf16_rne(r1), b2 = bf16_rne(r2);
-                    if (e & 1) {
-                        o1[e >> 1] |= b1 << 16;
-                        o2[e >> 1] |= b2 << 16;
-                    } else {
-                        o1[e >> 1] = b1;
-                        o2[e >> 1] = b2;
+                for (int k = 0; k < 8; ++k) {
+                    // frequencies f0+2k, f0+2k+1 at once: (x1, x2) = (x[j], x[j+D/2])
+                    // turned by δθ_j, with c1, s1 short enough for exact products
+                    const ulonglong2 C = cc[f0 / 2 + k], S = ss[f0 / 2 + k];
+                    const f2 x1 = f2_of_bf16x2(w1s[k]), x2 = f2_of_bf16x2(w2s[k]);
+                    const f2 x2n = f2_of_bf16x2(w2s[k] ^ 0x80008000u);
+                    const f2 r1 = f2_add(f2_fma(x1, C.x, f2_mul(x2n, S.x)),
+                                         f2_add(f2_fma(x1, C.y, f2_mul(x2n, S.y)),
+                                                f2_of_bits(a1[2 * k], a1[2 * k + 1])));
+                    const f2 r2 = f2_add(f2_fma(x2, C.x, f2_mul(x1, S.x)),
+                                         f2_add(f2_fma(x2, C.y, f2_mul(x1, S.y)),
+                                                f2_of_bits(a2[2 * k], a2[2 * k + 1])));
+                    chk = f2_fma(r1, 0ull, chk); // NaN if any result is Inf or NaN
+                    chk = f2_fma(r2, 0ull, chk);
+                    o1[k] = bf16x2_rne(r1);
+                    o2[k] = bf16x2_rne(r2);
+                }
+                if (__any_sync(0xFFFFFFFFu, f2_has_nan(chk))) {
+                    // Inf / NaN in the block (rare; whole warp, inputs read
+                    // again): elements with a non-finite input take plain
+                    // IEEE arithmetic, as the fp64 definition does
+                    uint32_t b1[16], b2[16];
+                    tmem_ld16(t_row + (uint32_t)f0, b1);
+                    tmem_ld16(t_row + (uint32_t)(f0 + G::HALF), b2);
+                    const uint16_t *x1h = reinterpret_cast<const uint16_t *>(xq) + f0;
+                    const uint16_t *x2h = x1h + G::HALF;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const uint32_t h1 = x1h[e], h2 = x2h[e];
+                        if (bf16_finite(h1) && bf16_finite(h2))
+                            continue;
+                        const int at = ((f0 + e) >> 1) * 4 + (e & 1);
+                        const float cs = cs_c[at] + cs_c[at + 2], sn = cs_s[at] + cs_s[at + 2];
+                        const float x1 = __uint_as_float(h1 << 16), x2 = __uint_as_float(h2 << 16);
+                        const uint32_t y1 = bf16_rne((x1 * cs - x2 * sn) + __uint_as_float(b1[e]));
+                        const uint32_t y2 = bf16_rne((x1 * sn + x2 * cs) + __uint_as_float(b2[e]));
+                        const int sh = 16 * (e & 1);
+                        o1[e >> 1] = (o1[e >> 1] & ~(0xFFFFu << sh)) | (y1 << sh);
+                        o2[e >> 1] = (o2[e >> 1] & ~(0xFFFFu << sh)) | (y2 << sh);
                     }
                 }
                 xq[f0 / 8] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
@@ -426,9 +515,9 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
                 const uint32_t ws[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
                 uint32_t o[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    o[e] = bf16_rne(bf16_lo(ws[e]) + __uint_as_float(a[2 * e])) |
-                           (bf16_rne(bf16_hi(ws[e]) + __uint_as_float(a[2 * e + 1])) << 16);
+                for (int k = 0; k < 8; ++k)
+                    o[k] = bf16x2_rne(f2_add(f2_of_bf16x2(ws[k]),
+                                             f2_of_bits(a[2 * k], a[2 * k + 1])));
                 xq[c16 / 8] = make_uint4(o[0], o[1], o[2], o[3]);
                 xq[c16 / 8 + 1] = make_uint4(o[4], o[5], o[6], o[7]);
             }
@@ -444,7 +533,10 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const uint32_t w1 = w1s[e], w2 = w2s[e];
-                    const float4 c0 = cs_s[f0 + 2 * e], c1 = cs_s[f0 + 2 * e + 1];
+                    const int at = ((f0 + 2 * e) >> 1) * 4;
+                    const float4 c0 = make_float4(cs_c[at], cs_c[at + 2], cs_s[at], cs_s[at + 2]);
+                    const float4 c1 =
+                        make_float4(cs_c[at + 1], cs_c[at + 3], cs_s[at + 1], cs_s[at + 3]);
                     o1[e] = rotate_one(w1 & 0xFFFFu, w2 & 0xFFFFu, c0, true, 0.0f) |
                             (rotate_one(w1 >> 16, w2 >> 16, c1, true, 0.0f) << 16);
                     o2[e] = rotate_one(w1 & 0xFFFFu, w2 & 0xFFFFu, c0, false, 0.0f) |

@@ -216,13 +216,24 @@ def test_relocate_nonfinite_inputs(orc):
 def test_fused_patch_nonfinite_inputs(orc, shape):
     wl, src, dst, dev = _reloc_case(shape, 265, num_reqs=1, chunks=2, lo=40, hi=60,
                                     deltas=[-555, 4321])
+    def plant(which, s, cols, b):
+        arr, view = (src.orc.rot, src.rot_view) if which == "rot" else (src.orc.copy,
+                                                                        src.copy_view)
+        arr[1, s, cols] = b
+        view[1, s, cols] = torch.tensor(int(np.array(b, np.uint16).view(np.int16)),
+                                        dtype=torch.int16).view(torch.bfloat16)
+
     specials = [0x7F80, 0xFF80, 0x7FC0, 0x7F81, 0x7F80]
     for k, b in enumerate(specials):
-        s = int(wl.src_slots[k])
-        col = (3 + 17 * k) % (src.H * src.d)
-        src.orc.rot[1, s, col] = b
-        src.rot_view[1, s, col] = torch.tensor(int(np.array(b, np.uint16).view(np.int16)),
-                                              dtype=torch.int16).view(torch.bfloat16)
+        plant("rot", int(wl.src_slots[k]), (3 + 17 * k) % (src.H * src.d), b)
+    # whole rotary half-heads at +-Inf: every frequency of the head, so the
+    # rotation meets both signs of the split cos / sin parts
+    h = src.d // 2
+    plant("rot", int(wl.src_slots[5]), slice(0, h), 0x7F80)
+    plant("rot", int(wl.src_slots[6]), slice(src.d + h, 2 * src.d) if src.H > 1
+          else slice(h, src.d), 0xFF80)
+    plant("copy", int(wl.src_slots[7]), slice(0, 8), 0x7F80)
+    plant("copy", int(wl.src_slots[7]), slice(8, 16), 0x7FC0)
     m = 8
     widths = (src.cd, src.H * src.d)
     us = [synth.f32_normal((L, wl.total_tokens, m), 266 + i, std=0.02) for i in range(2)]

@@ -59,10 +59,22 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sources_hash() -> str:
+# Sources that build each workload's dominant kernel (its own translation
+# unit, the shared device headers and the launch dispatch).
+_COMMON_SOURCES = ("kv_device.cuh", "kv_tiles.cuh", "kv_internal.h", "kv_launch.h", "kv_api.cu")
+KERNEL_SOURCES = {
+    "relocate_mla": ("kv_relocate.cu",) + _COMMON_SOURCES,
+    "splice_mla_128k": ("kv_splice.cu",) + _COMMON_SOURCES,
+    "relocate_gqa_patch": ("kv_patch_tc.cu",) + _COMMON_SOURCES,
+    "relocate_mla_patch": ("kv_patch_tc.cu",) + _COMMON_SOURCES,
+}
+
+
+def kernel_sources_hash(workload: str) -> str:
+    """sha256 (16 hex digits) of the sources that build `workload`'s kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "position_independent_mla_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(KERNEL_SOURCES[workload]):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -77,7 +89,7 @@ def recorded_traffic(workload: str):
                   if "=" in line and not line.startswith("#"))
     except OSError:
         return None
-    if kv.get("kernel_sources_sha256_16") != kernel_sources_hash():
+    if kv.get("kernel_sources_sha256_16") != kernel_sources_hash(workload):
         return None
     return float(kv["dram_bytes_per_launch"])
 
@@ -482,7 +494,8 @@ def run_relocate_mla_patch(args, rank, world, local):
         "config": {"workload": "irminsul-relocate-mla + fused rank-8 patch over the 576-wide row",
                    "tokens_per_step_per_gpu": T, "layers": L},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": recorded_traffic("relocate_mla_patch"),
                      "kernel": "patch_tc_kernel (c_KV: 256-column slices; k_pe: 64)",
                      "kernel_ms": kern_ms, "algorithmic_bytes_per_launch": bytes_launch},
         "clocks": clk, "gpu_launches": launches,

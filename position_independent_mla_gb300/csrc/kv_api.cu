@@ -211,10 +211,7 @@ kv_status relocate_impl(const kv_pool_desc *src, const kv_pool_desc *dst, int32_
         KV_CUDA(launch_patch_tc(rp, kind, stream));
         t_launches += patch_tc_launches(kind);
     } else {
-        if (patch_chunk_supported(rp))
-            KV_CUDA(launch_patch_chunks(rp, kind, stream));
-        else
-            KV_CUDA(launch_relocate(rp, kind, stream));
+        KV_CUDA(launch_relocate(rp, kind, stream));
         ++t_launches;
     }
     KV_CUDA(mark(t_ev_stop, stream));

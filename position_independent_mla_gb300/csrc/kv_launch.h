@@ -13,10 +13,8 @@ enum class RowKind {
 
 cudaError_t launch_delta_table(const TableParams &p, cudaStream_t stream);
 cudaError_t launch_relocate(const RelocParams &p, RowKind kind, cudaStream_t stream);
-// Patched relocation / in-place patch, one block per (chunk, layer), ranks <= 16.
-bool patch_chunk_supported(const RelocParams &p);
-cudaError_t launch_patch_chunks(const RelocParams &p, RowKind kind, cudaStream_t stream);
-// The same on the tensor cores (tcgen05), ranks <= 16.
+// Patched relocation / in-place patch on the tensor cores (tcgen05), ranks <= 16
+// (larger ranks take launch_relocate's per-element patch).
 bool patch_tc_supported(const RelocParams &p, RowKind kind);
 cudaError_t launch_patch_tc(const RelocParams &p, RowKind kind, cudaStream_t stream);
 int patch_tc_launches(RowKind kind); // kernels one launch_patch_tc issues

@@ -1050,9 +1050,261 @@ def run_reference(args, rank, world):
     }
 
 
+# ---------------------------------------------------------------------------
+# Workload: MLA sweep over chunk length x δ (relocate; splice with Δ = δ; patch)
+# ---------------------------------------------------------------------------
+
+SWEEP_MLA = dict(layers=61, chunk_lens=(16, 64, 256, 1024, 4096),
+                 deltas=(1, -1, 1000, -1000, 100000, -100000), num_reqs=8, req_tokens=131072,
+                 rank=8, base=10000.0, splice_seq=131072)
+# A small case of the same kernels (~1 GB on the device).
+SWEEP_MLA_SMALL = dict(SWEEP_MLA, layers=4, num_reqs=2, req_tokens=16384,
+                       deltas=(1, -1, 1000, -1000, 10000, -10000), splice_seq=16384)
+
+
+def _timed(call, K: int, W: int, prep=None):
+    """W untimed calls, then K timed ones, each after `prep` (untimed).
+    Returns (median call ms, median kernel ms, kernels launched while timed);
+    the kernel time is the library's own event pair around its main kernel."""
+    import position_independent_mla_gb300 as kv
+
+    for _ in range(W):
+        if prep:
+            prep()
+        call()
+    torch.cuda.synchronize()
+    call_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    kern_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    for a, b in call_ev + kern_ev:
+        a.record()
+        b.record()
+    launches = 0
+    for i in range(K):
+        if prep:
+            prep()
+        call_ev[i][0].record()
+        kv.kv_set_kernel_events(*kern_ev[i])
+        launches += call()
+        call_ev[i][1].record()
+    torch.cuda.synchronize()
+    kv.kv_set_kernel_events(None, None)
+    call_ms = float(np.median([a.elapsed_time(b) for a, b in call_ev]))
+    kern_ms = float(np.median([a.elapsed_time(b) for a, b in kern_ev]))
+    return call_ms, kern_ms, launches
+
+
+def check_patch_sample(rows_before, rows_after, idx, wl, u, v, m, orc) -> dict:
+    """Sampled parity of the standalone patch: each sampled (token, layer) row,
+    as stored before the call, patched by the oracle on a one-token problem."""
+    import oracle as O
+
+    out = {"copy_beyond": 0, "rot_beyond": 0, "exact": 0, "one_ulp": 0, "values": 0}
+    for k, (t, l) in enumerate(idx):
+        c = int(np.searchsorted(wl.tok_off, t, side="right") - 1)
+        pc, pr = np.zeros((1, 64, 512), np.uint16), np.zeros((1, 64, 64), np.uint16)
+        pc[0, 0], pr[0, 0] = rows_before[k, :512], rows_before[k, 512:]
+        pool = O.Pool(pc, pr, 64, 1, 64, 10000.0)
+        ut = u[l, t].cpu().numpy().reshape(1, 1, m)
+        vc = v[l, c].cpu().numpy().reshape(1, 1, 576, m)
+        assert orc.patch_apply(pool, [0, 1], [0], [0], [[0]],
+                               O.Patch(m, [ut, ut], [vc[:, :, :512], vc[:, :, 512:]])) == O.OK
+        for g, want, key in ((rows_after[k, :512], pool.copy[0, 0], "copy_beyond"),
+                             (rows_after[k, 512:], pool.rot[0, 0], "rot_beyond")):
+            r = ulp_stats(g, want)
+            out[key] += r["beyond"]
+            out["exact"] += r["exact"]
+            out["one_ulp"] += r["one_ulp"]
+            out["values"] += r["values"]
+    out["rows"] = len(idx)
+    return out
+
+
+def run_sweep_mla(args, rank, world, local):
+    """MLA, 61 layers: relocation at every (chunk length, δ) point; the
+    standalone rank-8 patch per chunk length; the splice with Δ = δ per δ (on
+    one sequence). Each measurement is the median of `--steps` calls."""
+    import position_independent_mla_gb300 as kv
+
+    cfg = SWEEP_MLA_SMALL if args.small else SWEEP_MLA
+    L, R, N, m, base = cfg["layers"], cfg["num_reqs"], cfg["req_tokens"], cfg["rank"], cfg["base"]
+    K, W = args.steps, args.warmup
+    peak, peak_kind = hbm_peak()
+    orc = None
+    if args.check and rank == 0:
+        import oracle as O
+        orc = O.get()
+    clocks = ClockSampler(local)
+    clocks.start()
+    launches = 0
+
+    # --- relocation: one registry of R*N distinct rows, one destination pool
+    wl0 = synth.fixed_chunk_workload(0, cfg["chunk_lens"][0], 0, R, N)
+    src = torch.empty((L, wl0.src_slots_total, MLA_ROW), dtype=torch.bfloat16, device="cuda")
+    fill_normal_(src, 5005 + 100 * rank)
+    dst = torch.zeros((L, wl0.dst_slots_total, MLA_ROW), dtype=torch.bfloat16, device="cuda")
+    sd = kv.pool_desc(src[..., :512], src[..., 512:], 64, 1, base)
+    dd = kv.pool_desc(dst[..., :512], dst[..., 512:], 64, 1, base)
+    reloc, wls = [], {}
+    for i, cl in enumerate(cfg["chunk_lens"]):
+        for j, delta in enumerate(cfg["deltas"]):
+            wl = synth.fixed_chunk_workload(5100 + 100 * rank + 10 * i + j, cl, delta, R, N)
+            wls.setdefault(cl, wl)
+            d = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).cuda()
+                 for k in ("tok_off", "src_slots", "chunk_req", "chunk_dst_pos", "delta",
+                           "block_tables")}
+            ws = kv.workspace(dd, wl.total_tokens, wl.num_chunks)
+
+            def call(wl=wl, d=d, ws=ws):
+                kv.kv_relocate(sd, dd, wl.num_chunks, wl.total_tokens, d["tok_off"],
+                               d["src_slots"], d["chunk_req"], d["chunk_dst_pos"], d["delta"],
+                               d["block_tables"], R, wl.block_tables.shape[1], None, ws)
+                return kv.kv_last_launch_count()
+
+            ms, kms, n = _timed(call, K, W)
+            launches += n
+            assert kv.kv_get_device_status(ws) == kv.KV_OK
+            T = wl.total_tokens
+            nbytes = T * (L * 2 * MLA_ROW_BYTES + 4)
+            pt = {"chunk_len": cl, "delta": delta, "chunks": wl.num_chunks, "ms": ms,
+                  "kernel_ms": kms, "tokens_per_s": T / (ms * 1e-3),
+                  "gbs": nbytes / (kms * 1e-3) / 1e9, "frac": nbytes / (kms * 1e-3) / 1e9 / peak,
+                  "bytes": nbytes}
+            if orc is not None:
+                pt["parity_sample"] = check_relocate_sample(
+                    dict(wl=wl, L=L, src=src, dst=dst, cfg=cfg), orc, n_rows=300, seed=7 + j)
+            reloc.append(pt)
+    del src
+    torch.cuda.empty_cache()
+
+    # --- standalone patch (in place on the relocated destination), per chunk length
+    patch = []
+    for i, cl in enumerate(cfg["chunk_lens"]):
+        wl = wls[cl]
+        T, C = wl.total_tokens, wl.num_chunks
+        g = torch.Generator(device="cuda")
+        g.manual_seed(5600 + 100 * rank + i)
+        u = torch.randn((L, T, m), generator=g, device="cuda").mul_(0.02)
+        v = torch.randn((L, C, 576, m), generator=g, device="cuda").mul_(0.02)
+        pd = kv.patch_desc(m, [u, u], [v[:, :, :512], v[:, :, 512:]])
+        d = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).cuda()
+             for k in ("tok_off", "chunk_req", "chunk_dst_pos", "block_tables")}
+        ws = kv.workspace(dd, T, C)
+
+        def call(wl=wl, d=d, ws=ws, pd=pd):
+            kv.kv_patch(dd, wl.num_chunks, wl.total_tokens, d["tok_off"], d["chunk_req"],
+                        d["chunk_dst_pos"], d["block_tables"], R, wl.block_tables.shape[1], pd, ws)
+            return kv.kv_last_launch_count()
+
+        pt = {"chunk_len": cl, "chunks": C}
+        if orc is not None:
+            rng = np.random.default_rng(31 + i)
+            idx = [(int(rng.integers(T)), int(rng.integers(L))) for _ in range(100)]
+
+            def rows(idx=idx, wl=wl):
+                out = []
+                for t, l in idx:
+                    c = int(np.searchsorted(wl.tok_off, t, side="right") - 1)
+                    p = int(wl.chunk_dst_pos[c]) + t - int(wl.tok_off[c])
+                    slot = int(wl.block_tables[wl.chunk_req[c], p // 64]) * 64 + p % 64
+                    out.append(synth.bits(dst[l, slot].cpu()))
+                return np.stack(out)
+
+            before = rows()
+            call()
+            pt["parity_sample"] = check_patch_sample(before, rows(), idx, wl, u, v, m, orc)
+        ms, kms, n = _timed(call, K, W)
+        launches += n
+        assert kv.kv_get_device_status(ws) == kv.KV_OK
+        nbytes = T * L * 2 * MLA_ROW_BYTES + T * L * m * 4 + C * L * 576 * m * 4
+        pt.update({"ms": ms, "kernel_ms": kms, "tokens_per_s": T / (ms * 1e-3),
+                   "gbs": nbytes / (kms * 1e-3) / 1e9,
+                   "frac": nbytes / (kms * 1e-3) / 1e9 / peak, "bytes": nbytes})
+        patch.append(pt)
+        del u, v, pd
+    del dst
+    torch.cuda.empty_cache()
+
+    # --- splice with Δ = δ on one sequence: n_R = max(16, 16 + δ), |S| = n_R - δ
+    n = cfg["splice_seq"]
+    max_blocks = (n + max(cfg["deltas"]) + 63) // 64
+    ss = synth.splice_seqs(5700 + 100 * rank, [n], max_blocks)
+    pool = torch.empty((L, ss.num_slots, MLA_ROW), dtype=torch.bfloat16, device="cuda")
+    fill_normal_(pool, 5701 + 100 * rank)
+    pristine = pool.clone()
+    desc = kv.pool_desc(pool[..., :512], pool[..., 512:], 64, 1, base)
+    bt = torch.from_numpy(ss.block_tables).cuda()
+    ws = kv.workspace(desc, n, 1)
+    splice = []
+    for j, delta in enumerate(cfg["deltas"]):
+        nr = max(16, 16 + delta)
+        span = nr - delta
+        rng = np.random.default_rng(5800 + 100 * rank + j)
+        s0 = int(rng.integers(0, n - span + 1))
+        d = synth.Directives(np.asarray([s0], np.int32), np.asarray([s0 + span], np.int32),
+                             np.asarray([nr], np.int32))
+        stub_c = torch.empty((L, nr, 512), dtype=torch.bfloat16, device="cuda")
+        stub_r = torch.empty((L, nr, 64), dtype=torch.bfloat16, device="cuda")
+        fill_normal_(stub_c, 5900 + 100 * rank + j)
+        fill_normal_(stub_r, 5950 + 100 * rank + j)
+        args_h = [torch.from_numpy(x.copy()) for x in (d.s_start, d.s_end, d.stub_len)]
+
+        def call(args_h=args_h, stub_c=stub_c, stub_r=stub_r):
+            lens = torch.tensor([n], dtype=torch.int32)
+            kv.kv_splice(desc, 1, bt, max_blocks, lens, *args_h, stub_c, stub_r,
+                         kv.KV_AMORTIZE, ws)
+            return kv.kv_last_launch_count()
+
+        ms, kms, k_l = _timed(call, K, W, prep=lambda: pool.copy_(pristine))
+        launches += k_l
+        assert kv.kv_get_device_status(ws) == kv.KV_OK
+        moved = (n - (s0 + span)) + nr
+        nbytes = moved * L * 2 * MLA_ROW_BYTES
+        pt = {"delta": delta, "stub_rows": nr, "removed": span, "s_start": s0,
+              "rows_moved": moved, "ms": ms, "kernel_ms": kms,
+              "tokens_per_s": moved / (ms * 1e-3), "gbs": nbytes / (kms * 1e-3) / 1e9,
+              "frac": nbytes / (kms * 1e-3) / 1e9 / peak, "bytes": nbytes,
+              "l2": "larger than L2" if nbytes > 2 * 129e6 else "L2-resident"}
+        if orc is not None:
+            pool.copy_(pristine)
+            call()
+            pt["parity_sample"] = check_splice_sample(
+                dict(L=L, S=1, ss=ss, cfg=cfg, rounds=[dict(d=d, stub_c=stub_c, stub_r=stub_r)],
+                     final_lens=np.asarray([n + delta]), pristine=pristine, pool=pool),
+                orc, n_rows=300, seed=13 + j)
+        splice.append(pt)
+        del stub_c, stub_r
+    clk = clocks.stop()
+
+    tot_tok = sum(p["chunks"] * p["chunk_len"] for p in reloc)
+    tot_ms = sum(p["ms"] for p in reloc)
+    tot_bytes = sum(p["bytes"] for p in reloc)
+    tot_kms = sum(p["kernel_ms"] for p in reloc)
+    achieved = tot_bytes / (tot_kms * 1e-3) / 1e9
+    return {
+        "metric": "relocated KV tokens/s (all layers)",
+        "value": tot_tok * world / (tot_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": tot_ms / len(reloc), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "impl": "ours",
+        "config": {"workload": f"mla-sweep: {L} layers, {R} requests x {N} tokens per "
+                               "relocation, chunk lengths x delta; splice with Delta = delta "
+                               f"on one {n}-token sequence; standalone rank-{m} patch",
+                   "value_is": "relocated tokens over all points / relocation time over all points",
+                   "relocate": reloc, "splice": splice, "patch": patch,
+                   "l2": "relocation and patch move >= 4 GB per call; splice points say"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "kernel": "relocate_kernel<MLA> over all sweep points",
+                     "kernel_ms": tot_kms / len(reloc)},
+        "e2e": None, "clocks": clk, "gpu_launches": launches,
+    }
+
+
 WORKLOADS = {"relocate-mla": run_relocate_mla, "splice-mla-128k": run_splice_mla_128k,
              "relocate-gqa-patch": run_relocate_gqa_patch, "splice-mla-4k": run_splice_mla_4k,
-             "relocate-mla-patch": run_relocate_mla_patch}
+             "relocate-mla-patch": run_relocate_mla_patch, "sweep-mla": run_sweep_mla}
 
 
 def main(argv=None):

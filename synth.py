@@ -138,6 +138,39 @@ def relocate_workload(seed: int, num_reqs: int, chunks_per_req: int, len_lo: int
         delta=delta, block_tables=bt, chunk_len=np.asarray(chunk_len, np.int32))
 
 
+def fixed_chunk_workload(seed: int, chunk_len: int, delta: int, num_reqs: int, req_tokens: int,
+                         block: int = BLOCK) -> RelocateWorkload:
+    """Relocation of ``num_reqs`` x ``req_tokens`` tokens in chunks of exactly
+    ``chunk_len`` tokens, every chunk with the same δ (a sweep point).  The
+    registry holds one distinct canonical chunk per relocated chunk, packed
+    back to back (chunks shorter than a block share blocks) over a random
+    block permutation, so the call reads every registry row once.  Each
+    request starts at a random offset inside its first destination block and
+    lays its chunks back to back; all of its block-table entries are real
+    blocks in a random permutation of the destination pool."""
+    assert req_tokens % chunk_len == 0
+    rng = np.random.default_rng(seed)
+    per_req = req_tokens // chunk_len
+    n_chunks = num_reqs * per_req
+    reg_blocks = (n_chunks * chunk_len + block - 1) // block
+    reg_perm = rng.permutation(reg_blocks).astype(np.int64)
+    order = rng.permutation(n_chunks).astype(np.int64)     # registry chunk of each chunk
+    pos = (order[:, None] * chunk_len + np.arange(chunk_len)[None, :]).reshape(-1)
+    src_slots = (reg_perm[pos // block] * block + pos % block).astype(np.int32)
+    chunk_req = np.repeat(np.arange(num_reqs), per_req).astype(np.int32)
+    bases = rng.integers(0, block, size=num_reqs)
+    chunk_dst_pos = (bases[chunk_req] +
+                     np.tile(np.arange(per_req) * chunk_len, num_reqs)).astype(np.int32)
+    max_blocks = (block - 1 + req_tokens + block - 1) // block
+    bt = rng.permutation(num_reqs * max_blocks).astype(np.int32).reshape(num_reqs, max_blocks)
+    return RelocateWorkload(
+        src_slots_total=reg_blocks * block, dst_slots_total=num_reqs * max_blocks * block,
+        tok_off=(np.arange(n_chunks + 1) * chunk_len).astype(np.int32), src_slots=src_slots,
+        chunk_req=chunk_req, chunk_dst_pos=chunk_dst_pos,
+        delta=np.full(n_chunks, delta, np.int32), block_tables=bt,
+        chunk_len=np.full(n_chunks, chunk_len, np.int32))
+
+
 # ---------------------------------------------------------------------------
 # Splice workloads (Leyline §2.1-§2.3)
 # ---------------------------------------------------------------------------

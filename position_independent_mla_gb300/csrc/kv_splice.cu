@@ -14,14 +14,18 @@
 // counter (so tickets are handed out in launch order, and every tile a block
 // waits for belongs to a block that is already running).  Every shift tile
 // owns a counter: the number of layers whose rows it has read, published
-// with a release store.  Layer by layer a block loads its rows; thread 0
-// makes sure (acquire, bounded) that the tiles it overwrites have read this
-// layer -- a value seen once covers all layers up to it, so a dependency far
-// behind costs one poll for the whole tile -- then one barrier, the block's
-// own counter is published, and the rows are stored.  The earliest
-// unfinished tile never waits on an unfinished one, so the protocol cannot
-// deadlock; the bound on each wait turns any unforeseen stall into
-// KV_ERR_TIMEOUT instead of a hang.
+// with a release store.  Layer by layer a block loads its rows and, once they
+// have landed, publishes its counter at once: reading needs nothing, since a
+// tile's source rows are overwritten only by itself and by later tiles.  Then
+// thread 0 makes sure (acquire, bounded) that the tiles it overwrites have
+// read this layer -- a value seen once covers all layers up to it, so a
+// dependency far behind costs one poll for the whole tile -- and after a
+// barrier the rows are stored.  Because reads are published before any wait,
+// a tile's wait chain runs back through at most one earlier tile per layer
+// (its length is bounded by the layer count, not by the number of tiles).
+// The earliest unfinished tile never waits on an unfinished one, so the
+// protocol cannot deadlock; the bound on each wait turns any unforeseen
+// stall into KV_ERR_TIMEOUT instead of a hang.
 #include "kv_launch.h"
 #include "kv_tiles.cuh"
 
@@ -141,6 +145,13 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
         const uint32_t f = fold_tile<G>(regs);
         if (p.total_tickets < 0)
             s_sink = f;
+        __syncthreads();
+        // layer l of this tile's source rows is in registers: publish it now,
+        // before waiting on anyone, so that a tile's progress never waits on
+        // the tiles behind it (its source rows are overwritten only by itself
+        // and by later tiles)
+        if (tid == 0 && shift)
+            st_release(p.flags + S.flag_base + k, (uint32_t)l + 1u);
         if (tid == 0 && !s_abort) {
             // the tiles this one overwrites must have read layer l
             for (int d = 0; d < 2; ++d) {
@@ -157,8 +168,6 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
             }
         }
         __syncthreads();
-        if (tid == 0 && shift)
-            st_release(p.flags + S.flag_base + k, (uint32_t)l + 1u); // layer l read
         if (!s_abort)
             store_tile<G, false>(pool_l, s_dst, regs, s_cs, 0, s_ident, none);
     }

@@ -251,6 +251,11 @@ __device__ __forceinline__ void st_release(uint32_t *p, uint32_t v)
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Spin until *flag != 0, for at most limit_ns of wall time and at most a
 // fixed number of polls (the poll cap bounds the wait even if the timer
 // misbehaves).  Returns false if the wait ran out.

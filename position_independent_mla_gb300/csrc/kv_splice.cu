@@ -13,14 +13,14 @@
 // at most two earlier tiles.  Each block takes a ticket from an atomic
 // counter (so tickets are handed out in launch order, and every tile a block
 // waits for belongs to a block that is already running).  Every shift tile
-// owns a counter: the number of layers whose rows it has read, published
-// with a release store.  Layer by layer a block loads its rows and, once they
-// have landed, publishes its counter at once: reading needs nothing, since a
-// tile's source rows are overwritten only by itself and by later tiles.  Then
-// thread 0 makes sure (acquire, bounded) that the tiles it overwrites have
-// read this layer -- a value seen once covers all layers up to it, so a
-// dependency far behind costs one poll for the whole tile -- and after a
-// barrier the rows are stored.  Because reads are published before any wait,
+// owns a counter of (layer, warp) reads, each warp adding one with a release
+// reduction once its loads of a layer have landed, so layer l is read when
+// the counter reaches 8 (l + 1).  A warp publishes at once: reading needs
+// nothing, since a tile's source rows are overwritten only by itself and by
+// later tiles.  Then thread 0 makes sure (acquire, bounded) that the tiles
+// it overwrites have read this layer -- a value seen once covers all layers
+// up to it, so a dependency far behind costs one poll for the whole tile --
+// and after one barrier the rows are stored.  Because reads are published before any wait,
 // a tile's wait chain runs back through at most one earlier tile per layer
 // (its length is bounded by the layer count, not by the number of tiles).
 // The earliest unfinished tile never waits on an unfinished one, so the
@@ -30,6 +30,8 @@
 #include "kv_tiles.cuh"
 
 namespace kvr {
+
+constexpr uint32_t kWarps = kThreads / 32;
 
 template <class G>
 __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const __grid_constant__ SpliceParams p)
@@ -145,21 +147,22 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
         const uint32_t f = fold_tile<G>(regs);
         if (p.total_tickets < 0)
             s_sink = f;
-        __syncthreads();
-        // layer l of this tile's source rows is in registers: publish it now,
-        // before waiting on anyone, so that a tile's progress never waits on
-        // the tiles behind it (its source rows are overwritten only by itself
-        // and by later tiles)
-        if (tid == 0 && shift)
-            st_release(p.flags + S.flag_base + k, (uint32_t)l + 1u);
+        // this warp's share of layer l is in registers: publish it now (one
+        // increment per warp), before waiting on anyone, so that a tile's
+        // progress never waits on the tiles behind it (its source rows are
+        // overwritten only by itself and by later tiles)
+        __syncwarp();
+        if (shift && (tid & 31) == 0)
+            red_release_add(p.flags + S.flag_base + k, 1u);
+        const uint32_t want = ((uint32_t)l + 1u) * kWarps; // every warp has read layer l
         if (tid == 0 && !s_abort) {
             // the tiles this one overwrites must have read layer l
             for (int d = 0; d < 2; ++d) {
-                if (s_dep[d] < 0 || s_seen[d] > (uint32_t)l)
+                if (s_dep[d] < 0 || s_seen[d] >= want)
                     continue;
-                const uint32_t seen = wait_count(p.flags + S.flag_base + s_dep[d], (uint32_t)l + 1u,
-                                                 p.wait_limit_ns);
-                if (seen <= (uint32_t)l) {
+                const uint32_t seen =
+                    wait_count(p.flags + S.flag_base + s_dep[d], want, p.wait_limit_ns);
+                if (seen < want) {
                     set_status(p.status, kStatusTimeout);
                     s_abort = 1;
                     break;

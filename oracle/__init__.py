@@ -149,6 +149,9 @@ class Oracle:
                                         C.POINTER(_Patch)]
         lib.kvo_splice.restype = i32
         lib.kvo_splice.argtypes = [C.POINTER(_Pool), i32, vp, i32, vp, vp, vp, vp, vp, vp, i32]
+        lib.kvo_splice_composed.restype = i32
+        lib.kvo_splice_composed.argtypes = [C.POINTER(_Pool), i32, i32, vp, i32, vp, vp, vp, vp,
+                                            vp, vp]
 
     # -- scalar / vector helpers ------------------------------------------
     def round_bf16(self, v: float) -> int:
@@ -223,6 +226,27 @@ class Oracle:
         return int(self._lib.kvo_splice(
             C.byref(pp), len(seq_lens), _ptr(bt), bt.shape[1], _ptr(seq_lens), _ptr(s_start),
             _ptr(s_end), _ptr(stub_len), _ptr(stub_copy), _ptr(stub_rot), int(mode)))
+
+
+    def splice_composed(self, pool: Pool, block_tables, seq_lens: np.ndarray, s_start, s_end,
+                        stub_len, stub_copy: Optional[np.ndarray],
+                        stub_rot: Optional[np.ndarray]) -> int:
+        """Several directives per sequence applied as one composed edit (one
+        bf16 rounding per row).  ``s_start``, ``s_end``, ``stub_len`` are
+        (num_dirs, num_seqs) int32 arrays, directive i in the indexing left by
+        directives before it; stub rows directive-major, then sequence."""
+        assert seq_lens.dtype == np.int32 and seq_lens.flags.c_contiguous
+        bt = _i32(block_tables)
+        s_start, s_end, stub_len = _i32(s_start), _i32(s_end), _i32(stub_len)
+        assert s_start.ndim == 2 and s_start.shape[1] == len(seq_lens)
+        assert s_end.shape == s_start.shape and stub_len.shape == s_start.shape
+        if stub_copy is not None:
+            assert stub_copy.dtype == np.uint16 and stub_copy.flags.c_contiguous
+            assert stub_rot.dtype == np.uint16 and stub_rot.flags.c_contiguous
+        pp = pool._c()
+        return int(self._lib.kvo_splice_composed(
+            C.byref(pp), len(seq_lens), s_start.shape[0], _ptr(bt), bt.shape[1], _ptr(seq_lens),
+            _ptr(s_start), _ptr(s_end), _ptr(stub_len), _ptr(stub_copy), _ptr(stub_rot)))
 
 
 _default: Optional[Oracle] = None

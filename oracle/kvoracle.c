@@ -474,3 +474,141 @@ int kvo_splice(kvo_pool *pool, int num_seqs, const int32_t *block_tables, int ma
     }
     return KVO_OK;
 }
+
+/* Several directives per sequence, composed (the multi-directive reading of
+ * Leyline §2.2-§2.3 with the closure R(a)R(b) = R(a+b)).  Sequence q receives
+ * num_dirs directives in order; directive i is given in the indexing that
+ * directives 0..i-1 produced, exactly as num_dirs successive kvo_splice calls
+ * would take it:
+ *   (s_start[i*num_seqs + q], s_end[i*num_seqs + q], stub_len[i*num_seqs + q]).
+ * Stub rows are stored directive by directive and, within a directive,
+ * sequence by sequence -- the stub arrays of the successive calls back to
+ * back: stub_copy [L][Σ stub_len][copy_dim], stub_rot [L][Σ stub_len][rot width].
+ * Instead of rounding to bf16 after every directive, the directives are
+ * applied to the ORIGIN of every logical row (an original row at position
+ * p0, or a stub row that directive i wrote at position p0); the final row at
+ * position p is then formed once from its origin, every rot head turned by
+ * R(p - p0), and rounded once.  Only the final length is checked against the
+ * block table's capacity (intermediate states are never stored). */
+typedef struct {
+    int64_t src;     /* >= 0: original position; < 0: stub row -1 - src */
+    int64_t written; /* position the row held when it was last rounded   */
+} kvo_origin;
+
+int kvo_splice_composed(kvo_pool *pool, int num_seqs, int num_dirs, const int32_t *block_tables,
+                        int max_blocks, int32_t *seq_lens, const int32_t *s_start,
+                        const int32_t *s_end, const int32_t *stub_len, const uint16_t *stub_copy,
+                        const uint16_t *stub_rot)
+{
+    if (!pool_ok(pool) || num_seqs < 0 || num_dirs < 0)
+        return KVO_ERR_INVALID;
+    int64_t total_stub = 0;
+    for (int q = 0; q < num_seqs; ++q) {
+        int64_t len = seq_lens[q];
+        if (len < 0)
+            return KVO_ERR_INVALID;
+        for (int i = 0; i < num_dirs; ++i) {
+            const int64_t a = s_start[(int64_t)i * num_seqs + q];
+            const int64_t b = s_end[(int64_t)i * num_seqs + q];
+            const int64_t nr = stub_len[(int64_t)i * num_seqs + q];
+            if (a < 0 || a > b || b > len || nr < 0)
+                return KVO_ERR_INVALID;
+            len += nr - (b - a);
+            total_stub += nr;
+        }
+        if (len > INT32_MAX)
+            return KVO_ERR_INVALID;
+        if ((len + pool->block_size - 1) / pool->block_size > max_blocks)
+            return KVO_ERR_CAPACITY;
+        const int32_t *bt = block_tables + (int64_t)q * max_blocks;
+        const int64_t hi = len > seq_lens[q] ? len : seq_lens[q];
+        for (int64_t p = 0; p < hi; ++p)
+            if (slot_of(pool, bt, max_blocks, p) < 0)
+                return KVO_ERR_RANGE;
+    }
+    if (total_stub > 0 && (!stub_copy || !stub_rot))
+        return KVO_ERR_INVALID;
+    const int L = pool->num_layers, cd = pool->copy_dim, rd = pool->rot_d, rh = pool->rot_heads;
+    const int rw = rot_width(pool);
+    for (int q = 0; q < num_seqs; ++q) {
+        /* the origins of the logical rows, directive by directive */
+        int64_t len = seq_lens[q], cap = len;
+        for (int i = 0; i < num_dirs; ++i)
+            cap += stub_len[(int64_t)i * num_seqs + q];
+        kvo_origin *cur = malloc((size_t)(cap > 0 ? cap : 1) * sizeof *cur);
+        kvo_origin *nxt = malloc((size_t)(cap > 0 ? cap : 1) * sizeof *nxt);
+        if (!cur || !nxt) {
+            free(cur);
+            free(nxt);
+            return KVO_ERR_INVALID;
+        }
+        for (int64_t p = 0; p < len; ++p) {
+            cur[p].src = p;
+            cur[p].written = p;
+        }
+        for (int i = 0; i < num_dirs; ++i) {
+            const int64_t a = s_start[(int64_t)i * num_seqs + q];
+            const int64_t b = s_end[(int64_t)i * num_seqs + q];
+            const int64_t nr = stub_len[(int64_t)i * num_seqs + q];
+            /* first stub row of (directive i, sequence q) */
+            int64_t base = 0;
+            for (int i2 = 0; i2 < num_dirs; ++i2)
+                for (int q2 = 0; q2 < num_seqs; ++q2)
+                    if (i2 < i || (i2 == i && q2 < q))
+                        base += stub_len[(int64_t)i2 * num_seqs + q2];
+            int64_t n = 0;
+            for (int64_t p = 0; p < a; ++p)
+                nxt[n++] = cur[p];
+            for (int64_t k = 0; k < nr; ++k) {
+                nxt[n].src = -1 - (base + k);
+                nxt[n].written = a + k;
+                ++n;
+            }
+            for (int64_t p = b; p < len; ++p)
+                nxt[n++] = cur[p];
+            kvo_origin *t = cur;
+            cur = nxt;
+            nxt = t;
+            len = n;
+        }
+        const int32_t *bt = block_tables + (int64_t)q * max_blocks;
+        uint16_t *nc = malloc((size_t)(len > 0 ? len : 1) * cd * sizeof *nc);
+        uint16_t *nrr = malloc((size_t)(len > 0 ? len : 1) * rw * sizeof *nrr);
+        if (!nc || !nrr) {
+            free(cur);
+            free(nxt);
+            free(nc);
+            free(nrr);
+            return KVO_ERR_INVALID;
+        }
+        for (int l = 0; l < L; ++l) {
+            for (int64_t p = 0; p < len; ++p) {
+                const uint16_t *sc, *sr;
+                if (cur[p].src >= 0) {
+                    const int64_t s = slot_of(pool, bt, max_blocks, cur[p].src);
+                    sc = copy_row(pool, l, s);
+                    sr = rot_row(pool, l, s);
+                } else {
+                    const int64_t row = -1 - cur[p].src;
+                    sc = stub_copy + ((int64_t)l * total_stub + row) * cd;
+                    sr = stub_rot + ((int64_t)l * total_stub + row) * rw;
+                }
+                memcpy(nc + p * cd, sc, (size_t)cd * sizeof *nc);
+                for (int h = 0; h < rh; ++h)
+                    kvo_rotate_bf16(sr + h * rd, nrr + p * rw + h * rd, rd, p - cur[p].written,
+                                    pool->rope_base);
+            }
+            for (int64_t p = 0; p < len; ++p) {
+                const int64_t s = slot_of(pool, bt, max_blocks, p);
+                memcpy(copy_row(pool, l, s), nc + p * cd, (size_t)cd * sizeof *nc);
+                memcpy(rot_row(pool, l, s), nrr + p * rw, (size_t)rw * sizeof *nrr);
+            }
+        }
+        free(cur);
+        free(nxt);
+        free(nc);
+        free(nrr);
+        seq_lens[q] = (int32_t)len;
+    }
+    return KVO_OK;
+}

@@ -151,3 +151,43 @@ def splice(copy, rot, block, heads, d, base, bt, seq_lens, s_start, s_end, stub_
         new_lens.append(n + delta)
         off += nr
     return pc, pr, new_lens
+
+
+def splice_composed(copy, rot, block, heads, d, base, bt, seq_lens, dirs, stub_copy, stub_rot):
+    """List-slicing restatement of several directives per sequence, composed.
+
+    ``dirs`` lists the directives in order as (s_start[S], s_end[S],
+    stub_len[S]), each in the indexing the previous ones left; stub rows are
+    stored directive by directive, then sequence by sequence.  The sequence is
+    first edited symbolically -- each entry remembers where its content came
+    from and the position it was written at -- and every final row is then
+    that content turned once by R(final position - written position)."""
+    pc, pr = copy.copy(), rot.copy()
+    L = copy.shape[0]
+    first_stub, off = {}, 0
+    for i, (_, _, nrs) in enumerate(dirs):
+        for q, nr in enumerate(nrs):
+            first_stub[(i, q)] = off
+            off += int(nr)
+    new_lens = []
+    for q in range(len(seq_lens)):
+        seq = [("old", p, p) for p in range(int(seq_lens[q]))]
+        for i, (starts, ends, nrs) in enumerate(dirs):
+            a, b, nr = int(starts[q]), int(ends[q]), int(nrs[q])
+            stub = [("stub", first_stub[(i, q)] + k, a + k) for k in range(nr)]
+            seq = seq[:a] + stub + seq[b:]
+        for l in range(L):
+            rows = []
+            for p, (kind, idx, written) in enumerate(seq):
+                if kind == "old":
+                    s = slot(bt[q], idx, block)
+                    cpy, rt = list(copy[l, s]), list(rot[l, s])
+                else:
+                    cpy, rt = list(stub_copy[l, idx]), list(stub_rot[l, idx])
+                rows.append((cpy, rotate_row(rt, heads, d, p - written, base)))
+            for p, (cpy, rt) in enumerate(rows):
+                s = slot(bt[q], p, block)
+                pc[l, s] = cpy
+                pr[l, s] = rt
+        new_lens.append(len(seq))
+    return pc, pr, new_lens

@@ -43,6 +43,9 @@ MUTANTS = [
      "kvo_round_bf16(kvo_bf16_to_f64(kvo_round_bf16(ex[i])) + patch_term(patch, 1, l, t, c, h * rd + i))", 0),
     ("relocate-ignores-copy-patch", "if (has_patch(patch, 0)) {\n                    for (int col = 0; col < cd; ++col)\n                        dc[col]",
      "if (0) {\n                    for (int col = 0; col < cd; ++col)\n                        dc[col]", 0),
+    ("composed-origin-position-zero", "cur[p].written = p;", "cur[p].written = 0;", 0),
+    ("composed-stub-never-rotated", "rd, p - cur[p].written,", "rd, cur[p].src >= 0 ? p - cur[p].written : 0,", 0),
+    ("composed-stub-rows-ignore-sequence", "if (i2 < i || (i2 == i && q2 < q))", "if (i2 < i)", 0),
 ]
 
 
@@ -68,6 +71,9 @@ def _pins():
         ("splice-forget", P.test_splice_forget_truncates_without_moving_data),
         ("splice-successive", P.test_successive_directives_round_between_calls),
         ("splice-brute", P.test_splice_brute_force_every_directive),
+        ("composed-single", P.test_composed_single_directive_is_the_splice),
+        ("composed-batch", P.test_composed_three_directives_batch_gqa),
+        ("composed-brute", P.test_composed_brute_force_two_directives),
     ]
 
 

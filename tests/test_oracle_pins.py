@@ -519,6 +519,169 @@ def test_successive_directives_round_between_calls(oracle):
     assert np.array_equal(pool.copy, c) and np.array_equal(pool.rot, r)
 
 
+# ---------------------------------------------------------------------------
+# Composed directives: every row moved once, rotated by its total shift,
+# rounded once (Leyline §2.2-§2.3 with R(a)R(b) = R(a+b))
+# ---------------------------------------------------------------------------
+
+def _stubs(seed, L, n, cd, rw):
+    sc = synth.bits(synth.bf16_normal((L, max(n, 1), cd), seed)).copy()
+    sr = synth.bits(synth.bf16_normal((L, max(n, 1), rw), seed + 1)).copy()
+    return np.ascontiguousarray(sc[:, :n]), np.ascontiguousarray(sr[:, :n])
+
+
+def _random_dirs(rng, lens, k, max_span, max_stub, cap):
+    """k directives per sequence, each valid in the indexing the previous left."""
+    cur = list(lens)
+    dirs = []
+    for _ in range(k):
+        a_s, b_s, n_s = [], [], []
+        for q, n in enumerate(cur):
+            a = int(rng.integers(0, n + 1))
+            b = int(rng.integers(a, min(n, a + max_span) + 1))
+            nr = int(rng.integers(0, max_stub + 1))
+            nr = min(nr, cap - (n - (b - a)))
+            a_s.append(a)
+            b_s.append(b)
+            n_s.append(nr)
+            cur[q] = n + nr - (b - a)
+        dirs.append((a_s, b_s, n_s))
+    return dirs
+
+
+def _dir_arrays(dirs):
+    return tuple(np.asarray([d[j] for d in dirs], np.int32) for j in range(3))
+
+
+def test_composed_single_directive_is_the_splice(oracle):
+    # with one directive the composed edit is the plain splice, bit for bit
+    rng = np.random.default_rng(101)
+    for seed, heads, d, cd in ((102, 1, 8, 8), (103, 2, 8, 16)):
+        lens = [13, 0, 21, 9]
+        ss, cp, rt = _splice_pool(seed, lens, 9, heads, d, cd)
+        dirs = _random_dirs(rng, lens, 1, 10, 8, 9 * 4)
+        s0, s1, nr = _dir_arrays(dirs)
+        sc, sr = _stubs(seed + 5, 2, int(nr.sum()), cd, heads * d)
+        p1 = O.Pool(cp.copy(), rt.copy(), 4, heads, d, 10000.0)
+        p2 = O.Pool(cp.copy(), rt.copy(), 4, heads, d, 10000.0)
+        l1, l2 = np.array(lens, np.int32), np.array(lens, np.int32)
+        assert oracle.splice(p1, ss.block_tables, l1, s0[0], s1[0], nr[0], sc, sr) == O.OK
+        assert oracle.splice_composed(p2, ss.block_tables, l2, s0, s1, nr, sc, sr) == O.OK
+        assert l1.tolist() == l2.tolist()
+        assert np.array_equal(p1.copy, p2.copy) and np.array_equal(p1.rot, p2.rot)
+
+
+def test_composed_brute_force_two_directives(oracle):
+    # many directive pairs on a 10-token cache, against symbolic list slicing
+    # with one complex rotation per row
+    n, maxb = 10, 7
+    ss, cp, rt = _splice_pool(111, [n], maxb)
+    rng = np.random.default_rng(112)
+    cases = 0
+    for _ in range(160):
+        dirs = _random_dirs(rng, [n], 2, 6, 6, maxb * 4)
+        s0, s1, nr = _dir_arrays(dirs)
+        sc, sr = _stubs(113, 2, int(nr.sum()), 8, 8)
+        pool = O.Pool(cp.copy(), rt.copy(), 4, 1, 8, 10000.0)
+        lens = np.array([n], np.int32)
+        assert oracle.splice_composed(pool, ss.block_tables, lens, s0, s1, nr, sc, sr) == O.OK
+        wc, wr, wl = ind.splice_composed(cp, rt, 4, 1, 8, 10000.0, ss.block_tables, [n], dirs,
+                                         sc, sr)
+        assert lens.tolist() == wl
+        assert np.array_equal(pool.copy, wc) and np.array_equal(pool.rot, wr)
+        cases += 1
+    assert cases == 160
+
+
+def test_composed_three_directives_batch_gqa(oracle):
+    lens = [17, 5, 0, 26]
+    ss, cp, rt = _splice_pool(121, lens, 12, heads=2, d=8, cd=16)
+    dirs = _random_dirs(np.random.default_rng(122), lens, 3, 9, 7, 12 * 4)
+    s0, s1, nr = _dir_arrays(dirs)
+    sc, sr = _stubs(123, 2, int(nr.sum()), 16, 16)
+    pool = O.Pool(cp.copy(), rt.copy(), 4, 2, 8, 10000.0)
+    seq = np.array(lens, np.int32)
+    assert oracle.splice_composed(pool, ss.block_tables, seq, s0, s1, nr, sc, sr) == O.OK
+    wc, wr, wl = ind.splice_composed(cp, rt, 4, 2, 8, 10000.0, ss.block_tables, lens, dirs, sc, sr)
+    assert seq.tolist() == wl
+    assert np.array_equal(pool.copy, wc) and np.array_equal(pool.rot, wr)
+
+
+def test_composed_differs_from_successive_calls_only_where_rows_rounded_twice(oracle):
+    # rows shifted by at most one of the directives are rotated once either
+    # way and agree bit for bit; rows shifted more than once are rounded once
+    # here and once per shift by successive calls
+    n = 40
+    ss, cp, rt = _splice_pool(131, [n], 16, d=16)
+    dirs = [([3], [9], [2]), ([20], [20], [5]), ([30], [34], [0])]
+    s0, s1, nr = _dir_arrays(dirs)
+    sc, sr = _stubs(132, 2, int(nr.sum()), 8, 16)
+    comp = O.Pool(cp.copy(), rt.copy(), 4, 1, 16, 10000.0)
+    lc = np.array([n], np.int32)
+    assert oracle.splice_composed(comp, ss.block_tables, lc, s0, s1, nr, sc, sr) == O.OK
+    succ = O.Pool(cp.copy(), rt.copy(), 4, 1, 16, 10000.0)
+    ls = np.array([n], np.int32)
+    off = 0
+    for a, b, k in dirs:
+        assert oracle.splice(succ, ss.block_tables, ls, a, b, k, np.ascontiguousarray(
+            sc[:, off:off + k[0]]), np.ascontiguousarray(sr[:, off:off + k[0]])) == O.OK
+        off += k[0]
+    assert lc.tolist() == ls.tolist() == [n + 2 - 6 + 5 - 4]
+    # shifts seen by each final position: track the edits symbolically
+    seq = [[0, 0] for _ in range(n)]                   # [nonzero shifts, 0]
+    for a, b, k in dirs:
+        delta = k[0] - (b[0] - a[0])
+        seq = seq[:a[0]] + [[0, 0] for _ in range(k[0])] + [
+            [c + (delta != 0), 0] for c, _ in seq[b[0]:]]
+    once = twice = 0
+    for p, (shifts, _) in enumerate(seq):
+        s = int(ss.block_tables[0, p // 4]) * 4 + p % 4
+        assert np.array_equal(comp.copy[:, s], succ.copy[:, s])
+        if shifts <= 1:
+            assert np.array_equal(comp.rot[:, s], succ.rot[:, s]), p
+            once += 1
+        else:
+            twice += 1
+    assert once > 0 and twice > 0
+
+
+def test_composed_insert_then_remove_restores_the_cache(oracle):
+    # insert 7 stub rows at 5, then remove exactly them: every row's total
+    # shift is 0, so the cache comes back bit for bit
+    n = 23
+    ss, cp, rt = _splice_pool(141, [n], 10)
+    sc, sr = _stubs(142, 2, 7, 8, 8)
+    pool = O.Pool(cp.copy(), rt.copy(), 4, 1, 8, 10000.0)
+    seq = np.array([n], np.int32)
+    s0, s1, nr = _dir_arrays([([5], [5], [7]), ([5], [12], [0])])
+    assert oracle.splice_composed(pool, ss.block_tables, seq, s0, s1, nr, sc, sr) == O.OK
+    assert seq.tolist() == [n]
+    assert np.array_equal(pool.copy, cp) and np.array_equal(pool.rot, rt)
+
+
+def test_composed_checks_final_capacity_and_each_directive(oracle):
+    ss, cp, rt = _splice_pool(151, [12], 4)              # capacity 16 tokens
+    sc, sr = _stubs(152, 2, 12, 8, 8)
+    pool = O.Pool(cp.copy(), rt.copy(), 4, 1, 8, 10000.0)
+    # grows to 22 in between, ends at 12: only the final length counts
+    s0, s1, nr = _dir_arrays([([0], [0], [10]), ([0], [10], [0])])
+    seq = np.array([12], np.int32)
+    assert oracle.splice_composed(pool, ss.block_tables, seq, s0, s1, nr, sc, sr) == O.OK
+    assert seq.tolist() == [12]
+    # ends at 18 > 16
+    s0, s1, nr = _dir_arrays([([0], [0], [10]), ([0], [4], [0])])
+    seq = np.array([12], np.int32)
+    assert oracle.splice_composed(pool, ss.block_tables, seq, s0, s1, nr, sc, sr) == O.ERR_CAPACITY
+    assert seq.tolist() == [12]
+    # the second directive's span lies beyond the length the first one left
+    before_c, before_r = pool.copy.copy(), pool.rot.copy()
+    s0, s1, nr = _dir_arrays([([2], [10], [0]), ([3], [5], [1])])
+    seq = np.array([12], np.int32)
+    assert oracle.splice_composed(pool, ss.block_tables, seq, s0, s1, nr, sc, sr) == O.ERR_INVALID
+    assert seq.tolist() == [12]
+    assert np.array_equal(pool.copy, before_c) and np.array_equal(pool.rot, before_r)
+
+
 def test_mla_row_split():
     # Irminsul §2.1: cKV is 89% of the MLA row, k_r 11%
     assert round(512 / 576 * 100) == 89 and round(64 / 576 * 100) == 11

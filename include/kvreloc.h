@@ -174,6 +174,64 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d
                     const void *d_stub_rot, kv_mode mode, void *d_workspace,
                     size_t workspace_bytes, kv_stream_t stream);
 
+/* Several directives per sequence applied as ONE in-place edit (Leyline
+ * §2.1-§2.3 composed with the closure R(a)R(b) = R(a+b)).  Sequence q gets
+ * num_dirs directives in order; directive i is
+ *   (h_s_start[i*num_seqs + q], h_s_end[i*num_seqs + q], h_stub_len[i*num_seqs + q])
+ * in the indexing that directives 0..i-1 left, exactly as num_dirs successive
+ * kv_splice calls would take them.  Stub rows are stored directive by
+ * directive and, within a directive, sequence by sequence (the stub arrays
+ * of the successive calls back to back):
+ *   d_stub_copy [L][Σ h_stub_len][copy_dim], d_stub_rot [L][Σ h_stub_len][rot width].
+ * Every row of the final sequence is written once, from its origin (an
+ * original row, or a stub row at the position its directive wrote it), its
+ * rotary part turned by the total shift it underwent and rounded once --
+ * where successive kv_splice calls round after every directive.  Rows whose
+ * total shift is 0 are not touched.  Only the final length is checked
+ * against max_blocks (KV_ERR_CAPACITY); h_seq_lens becomes the final
+ * lengths when the call returns KV_OK.  AMORTIZE semantics only.  The
+ * workspace size depends on the directives: kv_splice_composed_workspace_size
+ * (0 when the directives are invalid).  The plan is built on the host and
+ * copied into the workspace on `stream`. */
+size_t kv_splice_composed_workspace_size(const kv_pool_desc *pool, int32_t num_seqs,
+                                         int32_t num_dirs, const int32_t *h_seq_lens,
+                                         const int32_t *h_s_start, const int32_t *h_s_end,
+                                         const int32_t *h_stub_len);
+kv_status kv_splice_composed(const kv_pool_desc *pool, int32_t num_seqs, int32_t num_dirs,
+                             const int32_t *d_block_tables, int32_t max_blocks,
+                             int32_t *h_seq_lens, const int32_t *h_s_start, const int32_t *h_s_end,
+                             const int32_t *h_stub_len, const void *d_stub_copy,
+                             const void *d_stub_rot, void *d_workspace, size_t workspace_bytes,
+                             kv_stream_t stream);
+
+/* One tile of a composed splice plan, as kv_splice_composed_plan reports it:
+ * n (<= tile rows) rows moving from logical positions src_lo.. (or global
+ * stub rows src_lo.. when stub = 1) to logical positions dst_lo.. of
+ * sequence seq, rotary part turned by the shift h_deltas[unit] (unit = -1:
+ * no rotation).  dep[0..1] and dep[2..3] are two inclusive ranges of tiles
+ * (indices into the plan, all smaller than this tile's) whose source rows
+ * this tile's destination overlaps; -1 = none.  Tiles run in index order of
+ * their tickets. */
+typedef struct {
+    int64_t src_lo;
+    int64_t dst_lo;
+    int32_t n;
+    int32_t seq;
+    int32_t unit;
+    int32_t stub;
+    int32_t dep[4];
+} kv_splice_tile;
+
+/* The composed splice's plan, for inspection (host only, no device work):
+ * writes up to max_tiles tiles to h_tiles and up to max_units shifts to
+ * h_deltas (either may be NULL) and the counts to *n_tiles, *n_units.
+ * Argument errors as kv_splice_composed (capacity is not checked here). */
+kv_status kv_splice_composed_plan(const kv_pool_desc *pool, int32_t num_seqs, int32_t num_dirs,
+                                  const int32_t *h_seq_lens, const int32_t *h_s_start,
+                                  const int32_t *h_s_end, const int32_t *h_stub_len,
+                                  kv_splice_tile *h_tiles, int64_t max_tiles, int32_t *h_deltas,
+                                  int32_t max_units, int64_t *n_tiles, int32_t *n_units);
+
 /* Add the rank-m patch to stored rows in place (Kamera §2), one rounding per
  * value.  Chunks are described as in kv_relocate: the tokens of chunk c sit
  * at logical positions d_chunk_dst_pos[c] + i of request d_chunk_req[c]. */

@@ -7,6 +7,7 @@ missing, importing the binding's entry points raises.
 
     kv_relocate(src, dst, ...)   gather + R(δ) rotation (+ fused rank-m patch)
     kv_splice(pool, ...)         in-place Leyline AMORTIZE / FORGET directive
+    kv_splice_composed(pool, ...) several directives per sequence as one edit
     kv_patch(pool, ...)          in-place rank-m patch U_m V_mᵀ
 """
 from __future__ import annotations
@@ -64,6 +65,18 @@ class kv_patch_desc(C.Structure):
     ]
 
 
+class kv_splice_tile(C.Structure):
+    _fields_ = [
+        ("src_lo", C.c_int64),
+        ("dst_lo", C.c_int64),
+        ("n", C.c_int32),
+        ("seq", C.c_int32),
+        ("unit", C.c_int32),
+        ("stub", C.c_int32),
+        ("dep", C.c_int32 * 4),
+    ]
+
+
 _lib: Optional[C.CDLL] = None
 
 
@@ -85,6 +98,10 @@ def load(build_if_missing: bool = False) -> C.CDLL:
         "kv_relocate": (i32, [P, P, i32, i64, vp, vp, vp, vp, vp, vp, i32, i32, PP, vp, sz, vp]),
         "kv_splice": (i32, [P, i32, vp, i32, vp, vp, vp, vp, vp, vp, i32, vp, sz, vp]),
         "kv_patch": (i32, [P, i32, i64, vp, vp, vp, vp, i32, i32, PP, vp, sz, vp]),
+        "kv_splice_composed_workspace_size": (sz, [P, i32, i32, vp, vp, vp, vp]),
+        "kv_splice_composed": (i32, [P, i32, i32, vp, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "kv_splice_composed_plan": (i32, [P, i32, i32, vp, vp, vp, vp, vp, i64, vp, i32,
+                                          C.POINTER(i64), C.POINTER(i32)]),
         "kv_get_device_status": (i32, [vp, vp]),
         "kv_set_wait_limit_ns": (None, [i64]),
         "kv_check_wait_timeout": (i32, [vp, sz, i64, vp]),
@@ -218,6 +235,63 @@ def kv_splice(pool: kv_pool_desc, num_seqs: int, block_tables, max_blocks: int,
     if check:
         _check(st, "kv_splice")
     return st
+
+
+def _dirs(seq_lens, s_start, s_end, stub_len):
+    for t in (seq_lens, s_start, s_end, stub_len):
+        assert t.device.type == "cpu" and t.dtype == torch.int32 and t.is_contiguous()
+    assert s_start.dim() == 2 and s_start.shape[1] == seq_lens.numel()
+    assert s_end.shape == s_start.shape and stub_len.shape == s_start.shape
+    return int(seq_lens.numel()), int(s_start.shape[0])
+
+
+def kv_splice_composed_workspace_size(pool: kv_pool_desc, seq_lens, s_start, s_end,
+                                      stub_len) -> int:
+    """Bytes of workspace the composed splice of these directives needs (0:
+    invalid directives).  ``s_start``, ``s_end``, ``stub_len``: host int32
+    (num_dirs, num_seqs)."""
+    S, D = _dirs(seq_lens, s_start, s_end, stub_len)
+    return int(load().kv_splice_composed_workspace_size(
+        C.byref(pool), S, D, seq_lens.data_ptr(), s_start.data_ptr(), s_end.data_ptr(),
+        stub_len.data_ptr()))
+
+
+def kv_splice_composed(pool: kv_pool_desc, block_tables, max_blocks: int, seq_lens, s_start,
+                       s_end, stub_len, stub_copy, stub_rot, ws: Optional[torch.Tensor],
+                       stream=None, check: bool = True) -> int:
+    """Several directives per sequence as one in-place edit; ``seq_lens`` (host
+    int32) becomes the final lengths; directives host int32 (num_dirs,
+    num_seqs), directive i in the indexing the previous ones left; stubs
+    device bf16, directive-major then sequence."""
+    S, D = _dirs(seq_lens, s_start, s_end, stub_len)
+    st = load().kv_splice_composed(
+        C.byref(pool), S, D, _ptr(block_tables), int(max_blocks), seq_lens.data_ptr(),
+        s_start.data_ptr(), s_end.data_ptr(), stub_len.data_ptr(), _ptr(stub_copy),
+        _ptr(stub_rot), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(),
+        _stream(stream))
+    if check:
+        _check(st, "kv_splice_composed")
+    return st
+
+
+def kv_splice_composed_plan(pool: kv_pool_desc, seq_lens, s_start, s_end, stub_len):
+    """(status, tiles, deltas) of the composed splice's plan (host only):
+    tiles as a list of dicts with src_lo, dst_lo, n, seq, unit, stub, dep."""
+    S, D = _dirs(seq_lens, s_start, s_end, stub_len)
+    lib = load()
+    nt, nu = C.c_int64(0), C.c_int32(0)
+    args = (C.byref(pool), S, D, seq_lens.data_ptr(), s_start.data_ptr(), s_end.data_ptr(),
+            stub_len.data_ptr())
+    st = lib.kv_splice_composed_plan(*args, None, 0, None, 0, C.byref(nt), C.byref(nu))
+    if st != KV_OK:
+        return st, [], []
+    tiles = (kv_splice_tile * max(nt.value, 1))()
+    deltas = (C.c_int32 * max(nu.value, 1))()
+    st = lib.kv_splice_composed_plan(*args, tiles, nt.value, deltas, nu.value, C.byref(nt),
+                                     C.byref(nu))
+    out = [dict(src_lo=t.src_lo, dst_lo=t.dst_lo, n=t.n, seq=t.seq, unit=t.unit, stub=t.stub,
+                dep=list(t.dep)) for t in tiles[:nt.value]]
+    return st, out, list(deltas[:nu.value])
 
 
 def kv_patch(pool: kv_pool_desc, num_chunks: int, total_tokens: int, tok_off, chunk_req,

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <vector>
 
@@ -218,6 +219,209 @@ kv_status relocate_impl(const kv_pool_desc *src, const kv_pool_desc *dst, int32_
     return KV_OK;
 }
 
+
+// ---------------------------------------------------------------------------
+// Composed splice planning (host)
+// ---------------------------------------------------------------------------
+
+// A run of len logical rows whose content comes from src.. (original
+// positions, or global stub rows when `stub`) and was last rounded at
+// positions written..; within a run both advance with the position.
+struct Seg {
+    int64_t src, written, len;
+    bool stub;
+};
+
+struct ComposedPlan {
+    std::vector<SpliceTile> tiles;
+    std::vector<int32_t> deltas;   // δ-table unit -> shift
+    std::vector<int64_t> final_len; // per sequence
+    int64_t total_stub = 0;
+};
+
+// Pieces of the logical range [from, to) of `segs`, in order.
+void cut_range(const std::vector<Seg> &segs, int64_t from, int64_t to, std::vector<Seg> &out)
+{
+    int64_t pos = 0;
+    for (const Seg &g : segs) {
+        const int64_t lo = std::max(pos, from), hi = std::min(pos + g.len, to);
+        if (lo < hi)
+            out.push_back(Seg{g.src + (lo - pos), g.written + (lo - pos), hi - lo, g.stub});
+        pos += g.len;
+    }
+}
+
+// Inclusive run [first, last] of the tiles in tiles[b, e) -- sorted by
+// source position, ascending or descending, and non-overlapping -- whose
+// source rows meet [d, d + n), with `self` trimmed off the run's ends (a
+// tile may overwrite its own rows; no other position of self is possible).
+// Returns false when no other tile qualifies.
+bool overlapping_run(const std::vector<SpliceTile> &tiles, size_t b, size_t e, bool ascending,
+                     int64_t d, int64_t n, int64_t self, int32_t &first, int32_t &last)
+{
+    first = last = -1;
+    if (b >= e)
+        return false;
+    auto below = [&](const SpliceTile &u) { return u.src_lo + u.n <= d; }; // entirely before
+    auto above = [&](const SpliceTile &u) { return u.src_lo >= d + n; };  // entirely after
+    size_t lo, hi; // [lo, hi) meets the range
+    if (ascending) {
+        lo = (size_t)(std::partition_point(tiles.begin() + b, tiles.begin() + e, below) -
+                      tiles.begin());
+        hi = (size_t)(std::partition_point(tiles.begin() + lo, tiles.begin() + e,
+                                           [&](const SpliceTile &u) { return !above(u); }) -
+                      tiles.begin());
+    } else {
+        lo = (size_t)(std::partition_point(tiles.begin() + b, tiles.begin() + e, above) -
+                      tiles.begin());
+        hi = (size_t)(std::partition_point(tiles.begin() + lo, tiles.begin() + e,
+                                           [&](const SpliceTile &u) { return !below(u); }) -
+                      tiles.begin());
+    }
+    if (lo < hi && (int64_t)lo == self)
+        ++lo;
+    if (lo < hi && (int64_t)(hi - 1) == self)
+        --hi;
+    if (lo >= hi)
+        return false;
+    first = (int32_t)lo;
+    last = (int32_t)(hi - 1);
+    return true;
+}
+
+kv_status plan_composed(RowKind kind, int32_t num_seqs, int32_t num_dirs, int64_t capacity,
+                        const int32_t *lens, const int32_t *s0, const int32_t *s1,
+                        const int32_t *nr, ComposedPlan &plan)
+{
+    const int64_t T = tile_rows(kind);
+    // validate every directive in the indexing the previous ones leave
+    plan.total_stub = 0;
+    for (int32_t q = 0; q < num_seqs; ++q) {
+        int64_t len = lens[q];
+        if (len < 0)
+            return KV_ERR_INVALID_ARG;
+        for (int32_t i = 0; i < num_dirs; ++i) {
+            const int64_t k = (int64_t)i * num_seqs + q;
+            if (s0[k] < 0 || s0[k] > s1[k] || s1[k] > len || nr[k] < 0)
+                return KV_ERR_INVALID_ARG;
+            len += (int64_t)nr[k] - (s1[k] - s0[k]);
+            plan.total_stub += nr[k];
+        }
+        if (len > 0x7FFFFFFFll)
+            return KV_ERR_CAPACITY;
+        if (capacity >= 0 && std::max<int64_t>(len, lens[q]) > capacity)
+            return KV_ERR_CAPACITY;
+    }
+    std::map<int64_t, int32_t> unit_of;
+    auto unit = [&](int64_t shift) -> int32_t {
+        if (shift == 0)
+            return -1;
+        auto it = unit_of.find(shift);
+        if (it != unit_of.end())
+            return it->second;
+        const int32_t u = (int32_t)plan.deltas.size();
+        plan.deltas.push_back((int32_t)shift);
+        unit_of.emplace(shift, u);
+        return u;
+    };
+    int64_t stub_row = 0;
+    std::vector<int64_t> stub_first((size_t)num_dirs * num_seqs);
+    for (int32_t i = 0; i < num_dirs; ++i)
+        for (int32_t q = 0; q < num_seqs; ++q) {
+            stub_first[(size_t)i * num_seqs + q] = stub_row;
+            stub_row += nr[(int64_t)i * num_seqs + q];
+        }
+    plan.final_len.assign(num_seqs, 0);
+    for (int32_t q = 0; q < num_seqs; ++q) {
+        std::vector<Seg> segs;
+        int64_t len = lens[q];
+        if (len > 0)
+            segs.push_back(Seg{0, 0, len, false});
+        for (int32_t i = 0; i < num_dirs; ++i) {
+            const int64_t k = (int64_t)i * num_seqs + q;
+            std::vector<Seg> next;
+            cut_range(segs, 0, s0[k], next);
+            if (nr[k] > 0)
+                next.push_back(Seg{stub_first[(size_t)k], s0[k], nr[k], true});
+            cut_range(segs, s1[k], len, next);
+            segs.swap(next);
+            len += (int64_t)nr[k] - (s1[k] - s0[k]);
+        }
+        plan.final_len[q] = len;
+        // final positions and shifts; tiles: rows moving down (ascending),
+        // rows moving up (descending), stub rows
+        std::vector<int64_t> at(segs.size());
+        int64_t pos = 0;
+        for (size_t g = 0; g < segs.size(); ++g) {
+            at[g] = pos;
+            pos += segs[g].len;
+        }
+        const size_t base = plan.tiles.size();
+        for (size_t g = 0; g < segs.size(); ++g) {
+            const int64_t shift = at[g] - segs[g].written;
+            if (segs[g].stub || shift >= 0)
+                continue;
+            for (int64_t o = 0; o < segs[g].len; o += T)
+                plan.tiles.push_back(SpliceTile{segs[g].src + o, at[g] + o,
+                                                (int32_t)std::min(T, segs[g].len - o), q,
+                                                unit(shift), 0, {-1, -1, -1, -1}});
+        }
+        const size_t down_end = plan.tiles.size();
+        for (size_t g = segs.size(); g-- > 0;) {
+            const int64_t shift = at[g] - segs[g].written;
+            if (segs[g].stub || shift <= 0)
+                continue;
+            for (int64_t hi = segs[g].len; hi > 0; hi -= T) {
+                const int64_t lo = std::max<int64_t>(0, hi - T);
+                plan.tiles.push_back(SpliceTile{segs[g].src + lo, at[g] + lo, (int32_t)(hi - lo),
+                                                q, unit(shift), 0, {-1, -1, -1, -1}});
+            }
+        }
+        const size_t up_end = plan.tiles.size();
+        for (size_t g = 0; g < segs.size(); ++g) {
+            if (!segs[g].stub)
+                continue;
+            const int64_t shift = at[g] - segs[g].written;
+            for (int64_t o = 0; o < segs[g].len; o += T)
+                plan.tiles.push_back(SpliceTile{segs[g].src + o, at[g] + o,
+                                                (int32_t)std::min(T, segs[g].len - o), q,
+                                                unit(shift), 1, {-1, -1, -1, -1}});
+        }
+        // dependencies: the earlier tiles whose source rows each destination meets
+        for (size_t j = base; j < plan.tiles.size(); ++j) {
+            SpliceTile &tl = plan.tiles[j];
+            int32_t f, l;
+            int r = 0;
+            if (overlapping_run(plan.tiles, base, down_end, true, tl.dst_lo, tl.n, (int64_t)j, f, l)) {
+                tl.dep[2 * r] = f;
+                tl.dep[2 * r + 1] = l;
+                ++r;
+            }
+            if (overlapping_run(plan.tiles, down_end, up_end, false, tl.dst_lo, tl.n, (int64_t)j, f,
+                                l)) {
+                tl.dep[2 * r] = f;
+                tl.dep[2 * r + 1] = l;
+                ++r;
+            }
+            // every wait must point backwards, or the protocol could deadlock
+            for (int d = 0; d < 2 * r; ++d)
+                if (tl.dep[d] >= (int32_t)j)
+                    return KV_ERR_UNSUPPORTED;
+        }
+    }
+    if (plan.tiles.size() > 0x7FFFFFFFull)
+        return KV_ERR_CAPACITY;
+    return KV_OK;
+}
+
+// Workspace of a composed splice: header, δ-table, tiles, unit shifts, counters.
+size_t composed_bytes(const kv_pool_desc *pool, const ComposedPlan &plan)
+{
+    return kHeaderBytes + table_bytes(pool, (int64_t)plan.deltas.size()) +
+           align256(plan.tiles.size() * sizeof(SpliceTile)) +
+           align256(plan.deltas.size() * sizeof(int32_t)) + align256(plan.tiles.size() * 4u);
+}
+
 } // namespace
 
 extern "C" {
@@ -391,6 +595,145 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d
         KV_CUDA(mark(t_ev_stop, stream));
     for (int q = 0; q < num_seqs; ++q)
         h_seq_lens[q] += h_stub_len[q] - (h_s_end[q] - h_s_start[q]);
+    return KV_OK;
+}
+
+size_t kv_splice_composed_workspace_size(const kv_pool_desc *pool, int32_t num_seqs,
+                                         int32_t num_dirs, const int32_t *h_seq_lens,
+                                         const int32_t *h_s_start, const int32_t *h_s_end,
+                                         const int32_t *h_stub_len)
+{
+    RowKind kind;
+    if (!pool_ok(pool) || !row_kind(pool, &kind) || num_seqs < 0 || num_dirs < 0)
+        return 0;
+    if (num_seqs > 0 && (!h_seq_lens || (num_dirs > 0 && (!h_s_start || !h_s_end || !h_stub_len))))
+        return 0;
+    ComposedPlan plan;
+    if (plan_composed(kind, num_seqs, num_dirs, -1, h_seq_lens, h_s_start, h_s_end, h_stub_len,
+                      plan) != KV_OK)
+        return 0;
+    return composed_bytes(pool, plan);
+}
+
+kv_status kv_splice_composed(const kv_pool_desc *pool, int32_t num_seqs, int32_t num_dirs,
+                             const int32_t *d_block_tables, int32_t max_blocks,
+                             int32_t *h_seq_lens, const int32_t *h_s_start, const int32_t *h_s_end,
+                             const int32_t *h_stub_len, const void *d_stub_copy,
+                             const void *d_stub_rot, void *d_workspace, size_t workspace_bytes,
+                             kv_stream_t stream_)
+{
+    t_launches = 0;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (!pool_ok(pool))
+        return KV_ERR_INVALID_ARG;
+    RowKind kind;
+    if (!row_kind(pool, &kind))
+        return KV_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || num_dirs < 0)
+        return KV_ERR_INVALID_ARG;
+    if (num_seqs == 0 || num_dirs == 0)
+        return KV_OK;
+    if (!h_seq_lens || !h_s_start || !h_s_end || !h_stub_len || !d_block_tables || max_blocks <= 0)
+        return KV_ERR_INVALID_ARG;
+    ComposedPlan plan;
+    kv_status st = plan_composed(kind, num_seqs, num_dirs, (int64_t)max_blocks * pool->block_size,
+                                 h_seq_lens, h_s_start, h_s_end, h_stub_len, plan);
+    if (st != KV_OK)
+        return st;
+    if (plan.total_stub > 0 && (!d_stub_copy || !d_stub_rot || !aligned16(d_stub_copy) ||
+                                !aligned16(d_stub_rot)))
+        return KV_ERR_INVALID_ARG;
+    if ((st = ws_ok(d_workspace, workspace_bytes, composed_bytes(pool, plan))) != KV_OK)
+        return st;
+
+    char *w = static_cast<char *>(d_workspace);
+    uint32_t *status = reinterpret_cast<uint32_t *>(w);
+    const size_t tbytes = table_bytes(pool, (int64_t)plan.deltas.size());
+    float4 *table = reinterpret_cast<float4 *>(w + kHeaderBytes);
+    SpliceTile *tiles = reinterpret_cast<SpliceTile *>(w + kHeaderBytes + tbytes);
+    const size_t tiles_bytes = align256(plan.tiles.size() * sizeof(SpliceTile));
+    int32_t *deltas = reinterpret_cast<int32_t *>(w + kHeaderBytes + tbytes + tiles_bytes);
+    uint32_t *flags = reinterpret_cast<uint32_t *>(
+        w + kHeaderBytes + tbytes + tiles_bytes + align256(plan.deltas.size() * sizeof(int32_t)));
+    KV_CUDA(cudaMemsetAsync(w, 0, kHeaderBytes, stream));
+    if (!plan.tiles.empty()) {
+        // the plan is copied from pageable host memory: the call returns once
+        // the driver holds its own copy, so the vectors may go out of scope
+        KV_CUDA(cudaMemcpyAsync(tiles, plan.tiles.data(), plan.tiles.size() * sizeof(SpliceTile),
+                                cudaMemcpyHostToDevice, stream));
+        KV_CUDA(cudaMemsetAsync(flags, 0, plan.tiles.size() * 4u, stream));
+    }
+    if (!plan.deltas.empty()) {
+        KV_CUDA(cudaMemcpyAsync(deltas, plan.deltas.data(), plan.deltas.size() * sizeof(int32_t),
+                                cudaMemcpyHostToDevice, stream));
+        TableParams tp{};
+        tp.d_delta = deltas;
+        tp.units = (int32_t)plan.deltas.size();
+        tp.half = pool->rot_head_dim / 2;
+        tp.head_dim = pool->rot_head_dim;
+        tp.base = pool->rope_base;
+        tp.table = table;
+        KV_CUDA(launch_delta_table(tp, stream));
+        ++t_launches;
+    }
+    if (!plan.tiles.empty()) {
+        ComposedParams cp{};
+        cp.pool = view_of(pool);
+        cp.block_tables = d_block_tables;
+        cp.max_blocks = max_blocks;
+        cp.stub_copy = static_cast<const char *>(d_stub_copy);
+        cp.stub_rot = static_cast<const char *>(d_stub_rot);
+        cp.total_stub = plan.total_stub;
+        cp.tiles = tiles;
+        cp.table = table;
+        cp.status = status;
+        cp.ticket = status + 1;
+        cp.flags = flags;
+        cp.num_tiles = (int64_t)plan.tiles.size();
+        cp.wait_limit_ns = g_wait_limit_ns.load();
+        KV_CUDA(mark(t_ev_start, stream));
+        KV_CUDA(launch_splice_composed(cp, kind, stream));
+        KV_CUDA(mark(t_ev_stop, stream));
+        ++t_launches;
+    }
+    for (int32_t q = 0; q < num_seqs; ++q)
+        h_seq_lens[q] = (int32_t)plan.final_len[q];
+    return KV_OK;
+}
+
+kv_status kv_splice_composed_plan(const kv_pool_desc *pool, int32_t num_seqs, int32_t num_dirs,
+                                  const int32_t *h_seq_lens, const int32_t *h_s_start,
+                                  const int32_t *h_s_end, const int32_t *h_stub_len,
+                                  kv_splice_tile *h_tiles, int64_t max_tiles, int32_t *h_deltas,
+                                  int32_t max_units, int64_t *n_tiles, int32_t *n_units)
+{
+    static_assert(sizeof(kv_splice_tile) == sizeof(SpliceTile), "tile layout");
+    if (!pool_ok(pool))
+        return KV_ERR_INVALID_ARG;
+    RowKind kind;
+    if (!row_kind(pool, &kind))
+        return KV_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || num_dirs < 0 || !n_tiles || !n_units)
+        return KV_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!h_seq_lens || (num_dirs > 0 && (!h_s_start || !h_s_end || !h_stub_len))))
+        return KV_ERR_INVALID_ARG;
+    ComposedPlan plan;
+    if (num_dirs > 0) {
+        const kv_status st = plan_composed(kind, num_seqs, num_dirs, -1, h_seq_lens, h_s_start,
+                                           h_s_end, h_stub_len, plan);
+        if (st != KV_OK)
+            return st;
+    }
+    *n_tiles = (int64_t)plan.tiles.size();
+    *n_units = (int32_t)plan.deltas.size();
+    if (h_tiles)
+        std::memcpy(h_tiles, plan.tiles.data(),
+                    std::min<size_t>(plan.tiles.size(), (size_t)std::max<int64_t>(max_tiles, 0)) *
+                        sizeof(SpliceTile));
+    if (h_deltas)
+        std::memcpy(h_deltas, plan.deltas.data(),
+                    std::min<size_t>(plan.deltas.size(), (size_t)std::max<int32_t>(max_units, 0)) *
+                        sizeof(int32_t));
     return KV_OK;
 }
 

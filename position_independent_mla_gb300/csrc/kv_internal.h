@@ -86,6 +86,38 @@ struct SpliceParams {
     SpliceSeq seq[kMaxSeqsPerLaunch];
 };
 
+// One tile of a composed splice (several directives per sequence applied as
+// one edit): up to T rows that move from src_lo.. to dst_lo.. (logical
+// positions of sequence `seq`, or stub rows when `stub`), turned by the
+// δ-table row `unit` (-1: no rotation).  dep[0..1] and dep[2..3] are two
+// inclusive ranges of earlier tiles whose source rows this tile's
+// destination overlaps (-1: none).
+struct SpliceTile {
+    int64_t src_lo;
+    int64_t dst_lo;
+    int32_t n;
+    int32_t seq;
+    int32_t unit;
+    int32_t stub;
+    int32_t dep[4];
+};
+
+struct ComposedParams {
+    PoolView pool;
+    const int32_t *block_tables;
+    int32_t max_blocks;
+    const char *stub_copy; // [L][total_stub][copy_dim] bf16
+    const char *stub_rot;  // [L][total_stub][rot width] bf16
+    int64_t total_stub;
+    const SpliceTile *tiles; // [num_tiles], in ticket order
+    const float4 *table;     // [units][head_dim/2]
+    uint32_t *status;
+    uint32_t *ticket;
+    uint32_t *flags; // [num_tiles] (layer, warp) read counters
+    int64_t num_tiles;
+    int64_t wait_limit_ns;
+};
+
 struct TableParams {
     const int32_t *d_delta;             // per-unit shifts in device memory, or ...
     int32_t h_delta[kMaxSeqsPerLaunch]; // ... carried in the launch (d_delta == nullptr)

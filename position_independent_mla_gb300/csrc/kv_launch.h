@@ -20,6 +20,8 @@ cudaError_t launch_patch_tc(const RelocParams &p, RowKind kind, cudaStream_t str
 int patch_tc_launches(RowKind kind); // kernels one launch_patch_tc issues
 // Launches one ticketed block per tile; `blocks` = p.total_tickets.
 cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stream);
+// Composed splice: one ticketed block per tile of p.tiles.
+cudaError_t launch_splice_composed(const ComposedParams &p, RowKind kind, cudaStream_t stream);
 cudaError_t launch_wait_check(uint32_t *flag, uint32_t *status, int64_t limit_ns,
                               cudaStream_t stream);
 

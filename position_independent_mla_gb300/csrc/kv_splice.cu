@@ -191,6 +191,128 @@ cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stre
 }
 
 // ---------------------------------------------------------------------------
+// Composed splice: several directives per sequence as one in-place edit.
+//
+// The host turns the directives into a table of tiles (each: T rows moving by
+// one constant shift, or stub rows landing at their final positions) ordered
+// so that every tile a tile overwrites comes earlier: rows moving down in
+// ascending order, rows moving up in descending order, stubs last (the map
+// is monotone, so rows moving down and rows moving up never overlap).  The
+// protocol is the splice's: tickets, per-warp release counts of the layers
+// read, bounded acquire waits on the (at most two ranges of) earlier tiles a
+// tile overwrites, one barrier per layer.  Every row is read once and rounded
+// once, its rotary part turned by its total shift.
+// ---------------------------------------------------------------------------
+
+template <class G>
+__global__ void __launch_bounds__(kThreads, G::kMinBlocks)
+splice_composed_kernel(const __grid_constant__ ComposedParams p)
+{
+    __shared__ uint32_t s_ticket;
+    __shared__ volatile int32_t s_abort;
+    __shared__ uint32_t s_min[2]; // smallest count seen over each dependency range
+    __shared__ int64_t s_src[G::T];
+    __shared__ int64_t s_dst[G::T];
+    __shared__ int32_t s_ident[G::T];
+    __shared__ float4 s_cs[G::kHalf];
+    __shared__ uint32_t s_sink;
+
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        s_ticket = atomicAdd(p.ticket, 1u);
+        s_abort = 0;
+        s_min[0] = s_min[1] = 0u;
+    }
+    __syncthreads();
+    const int64_t t = s_ticket;
+    if (t >= p.num_tiles)
+        return;
+    const SpliceTile tile = p.tiles[t];
+    const int32_t *bt = p.block_tables + (int64_t)tile.seq * p.max_blocks;
+    const int32_t B = p.pool.block;
+    const int64_t nb = p.pool.num_blocks;
+    const int L = p.pool.num_layers;
+    if (tid < G::T) {
+        int64_t src = -1, dst = -1;
+        if (tid < tile.n) {
+            src = tile.stub ? tile.src_lo + tid : slot_of(bt, p.max_blocks, B, nb, tile.src_lo + tid);
+            dst = slot_of(bt, p.max_blocks, B, nb, tile.dst_lo + tid);
+            if (src < 0 || dst < 0 || (tile.stub && src >= p.total_stub)) {
+                set_status(p.status, kStatusOutOfRange);
+                src = dst = -1;
+            }
+        }
+        s_src[tid] = src;
+        s_dst[tid] = dst;
+        s_ident[tid] = tile.unit < 0;
+    }
+    if (tile.unit >= 0)
+        for (int j = tid; j < G::kHalf; j += kThreads)
+            s_cs[G::cs_index(j)] = p.table[(int64_t)tile.unit * G::kHalf + j];
+    __syncthreads();
+
+    const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;
+    PatchAt none{nullptr, 0, nullptr, nullptr};
+    for (int l = 0; l < L; ++l) {
+        const RowsAt pool_l{p.pool.copy + l * p.pool.copy_ls, p.pool.copy_ss,
+                            p.pool.rot + l * p.pool.rot_ls, p.pool.rot_ss};
+        const RowsAt from = tile.stub ? RowsAt{p.stub_copy + l * p.total_stub * copy_row_bytes,
+                                               copy_row_bytes,
+                                               p.stub_rot + l * p.total_stub * rot_row_bytes,
+                                               rot_row_bytes}
+                                      : pool_l;
+        TileRegs<G> regs;
+        if (!s_abort)
+            load_tile<G>(from, s_src, regs);
+        else
+            regs = TileRegs<G>{};
+        const uint32_t f = fold_tile<G>(regs);
+        if (p.num_tiles < 0)
+            s_sink = f;
+        // this warp's share of layer l is read: publish before waiting
+        __syncwarp();
+        if (!tile.stub && (tid & 31) == 0)
+            red_release_add(p.flags + t, 1u);
+        const uint32_t want = ((uint32_t)l + 1u) * kWarps;
+        if (tid == 0 && !s_abort) {
+            for (int r = 0; r < 2 && !s_abort; ++r) {
+                const int32_t lo = tile.dep[2 * r], hi = tile.dep[2 * r + 1];
+                if (lo < 0 || s_min[r] >= want)
+                    continue;
+                uint32_t mn = 0xFFFFFFFFu;
+                for (int32_t j = lo; j <= hi; ++j) {
+                    const uint32_t seen = wait_count(p.flags + j, want, p.wait_limit_ns);
+                    if (seen < want) {
+                        set_status(p.status, kStatusTimeout);
+                        s_abort = 1;
+                        break;
+                    }
+                    mn = min(mn, seen);
+                }
+                s_min[r] = mn;
+            }
+        }
+        __syncthreads();
+        if (!s_abort)
+            store_tile<G, false>(pool_l, s_dst, regs, s_cs, 0, s_ident, none);
+    }
+}
+
+cudaError_t launch_splice_composed(const ComposedParams &p, RowKind kind, cudaStream_t stream)
+{
+    if (p.num_tiles == 0)
+        return cudaSuccess;
+    if (p.num_tiles > 0x7FFFFFFFll)
+        return cudaErrorInvalidConfiguration;
+    const unsigned blocks = (unsigned)p.num_tiles;
+    if (kind == RowKind::Mla)
+        splice_composed_kernel<GeoMla><<<blocks, kThreads, 0, stream>>>(p);
+    else
+        splice_composed_kernel<GeoGqa><<<blocks, kThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Failure-path check: the same bounded wait on a flag nothing sets.
 // ---------------------------------------------------------------------------
 

@@ -516,12 +516,12 @@ SPLICE_128K = dict(layers=61, num_seqs=8, seq_len=131072, rounds=4, span_lo=8192
 SPLICE_128K_SMALL = dict(SPLICE_128K, num_seqs=1, seq_len=32768, span_lo=2048, span_hi=8192)
 
 
-def build_splice(rank: int, cfg, device: str = "cuda"):
+def build_splice(rank: int, cfg, device: str = "cuda", aligned: bool = False):
     import position_independent_mla_gb300 as kv
 
     c = cfg
     L, S, n = c["layers"], c["num_seqs"], c["seq_len"]
-    max_blocks = (n + 63) // 64          # spans (>= 8K) outgrow stubs (<= 64): sequences shrink
+    max_blocks = (n + 63) // 64          # spans (>= 8K) outgrow stubs: sequences shrink
     ss = synth.splice_seqs(3003 + 100 * rank, [n] * S, max_blocks)
     pool = torch.empty((L, ss.num_slots, MLA_ROW), dtype=torch.bfloat16, device=device)
     fill_normal_(pool, 3003 + 100 * rank)
@@ -530,8 +530,12 @@ def build_splice(rank: int, cfg, device: str = "cuda"):
     lens = ss.seq_lens.copy()
     rounds = []
     for r in range(c["rounds"]):
-        d = synth.random_directives(3100 + 100 * rank + r, lens, c["span_lo"], c["span_hi"],
-                                    c["stub_lo"], c["stub_hi"])
+        if aligned:   # whole blocks: U[1, 4] stub blocks
+            d = synth.random_aligned_directives(3100 + 100 * rank + r, lens, c["span_lo"],
+                                                c["span_hi"], 1, 4)
+        else:
+            d = synth.random_directives(3100 + 100 * rank + r, lens, c["span_lo"], c["span_hi"],
+                                        c["stub_lo"], c["stub_hi"])
         tot = int(d.stub_len.sum())
         stub_c = torch.empty((L, tot, 512), dtype=torch.bfloat16, device=device)
         stub_r = torch.empty((L, tot, 64), dtype=torch.bfloat16, device=device)
@@ -548,22 +552,23 @@ def build_splice(rank: int, cfg, device: str = "cuda"):
                 L=L, S=S, final_lens=lens, cfg=c, max_blocks=max_blocks)
 
 
-def splice_step(st, stream=None):
+def splice_step(st, stream=None, mode=None):
     """All directive rounds on the restored cache; returns kernels launched."""
     import position_independent_mla_gb300 as kv
 
+    mode = kv.KV_AMORTIZE if mode is None else mode
     lens = torch.from_numpy(st["ss"].seq_lens.copy())
     launches = 0
     for rd in st["rounds"]:
         s0, s1, nr = rd["args"]
         kv.kv_splice(st["desc"], st["S"], st["bt"], st["max_blocks"], lens, s0, s1, nr,
-                     rd["stub_c"], rd["stub_r"], kv.KV_AMORTIZE, st["ws"], stream=stream)
+                     rd["stub_c"], rd["stub_r"], mode, st["ws"], stream=stream)
         launches += kv.kv_last_launch_count()
     return launches, lens
 
 
 def check_splice_sample(st, orc, n_rows: int = 2000, seed: int = 11,
-                        composed: bool = False) -> dict:
+                        composed: bool = False, final_bt=None) -> dict:
     """Sampled parity at full size: random (sequence, final position, layer)
     rows after all directive rounds, each traced back through the rounds to
     its origin (an original row or a stub row) and compared with the oracle's
@@ -597,6 +602,8 @@ def check_splice_sample(st, orc, n_rows: int = 2000, seed: int = 11,
         if origin is None:
             origin = ("pool", p)
         slot = lambda pos: int(bt[q, pos // 64]) * 64 + pos % 64
+        fbt = bt if final_bt is None else final_bt   # the block table after the edit
+        final_slot = int(fbt[q, p_final // 64]) * 64 + p_final % 64
         if origin[0] == "pool":
             row = st["pristine"][l, slot(origin[1])]
             oc, orr = row[:512], row[512:]
@@ -612,7 +619,7 @@ def check_splice_sample(st, orc, n_rows: int = 2000, seed: int = 11,
                 or_b = orc.rotate_bf16(or_b, delta, base)
         want_c.append(oc_b)
         want_r.append(or_b)
-        have_idx.append((l, slot(p_final)))
+        have_idx.append((l, final_slot))
     li = torch.tensor([x[0] for x in have_idx], device="cuda")
     si = torch.tensor([x[1] for x in have_idx], device="cuda")
     got = synth.bits(st["pool"][li, si].cpu())
@@ -714,6 +721,72 @@ def run_splice_mla_128k(args, rank, world, local):
     if args.check and rank == 0:
         import oracle as O
         out["parity_sample"] = check_splice_sample(st, O.get())
+    return out
+
+
+def run_splice_mla_128k_remap(args, rank, world, local):
+    """The 128K-context workload with block-aligned directives (spans of
+    U[8192, 32768] tokens rounded to whole blocks at block-aligned offsets,
+    stubs of 1-4 blocks), applied with KV_AMORTIZE_REMAP: downstream rows stay
+    in their blocks, the block-table rows are permuted and only the rotary
+    part is rewritten.  Timed against KV_AMORTIZE on the same directives;
+    before each step the cache and the block tables are restored, untimed."""
+    import position_independent_mla_gb300 as kv
+
+    cfg = SPLICE_128K_SMALL if args.small else SPLICE_128K
+    st = build_splice(rank, cfg, aligned=True)
+    L, R, S, K, W = st["L"], len(st["rounds"]), st["S"], args.steps, args.warmup
+    bt0 = st["bt"].clone()
+
+    def restore():
+        st["pool"].copy_(st["pristine"])
+        st["bt"].copy_(bt0)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    ms, kms, launches = _timed(lambda: splice_step(st, mode=kv.KV_AMORTIZE_REMAP)[0], K, W,
+                               prep=restore)
+    amortize_ms, _, _ = _timed(lambda: splice_step(st)[0], K, W, prep=restore)
+    barrier(world)
+    clk = clocks.stop()
+    assert kv.kv_get_device_status(st["ws"]) == kv.KV_OK
+    ms = max_over_ranks(ms, world)
+    # rows whose rotary part is rewritten in place (downstream) and stub rows
+    down = sum(int(np.sum(rd["lens_before"] - rd["d"].s_end)) for rd in st["rounds"])
+    stub = sum(int(np.sum(rd["d"].stub_len)) for rd in st["rounds"])
+    nbytes = down * L * 2 * 128 + stub * L * 2 * MLA_ROW_BYTES
+    moved = down + stub
+    peak, peak_kind = hbm_peak()
+    out = {
+        "metric": "relocated KV tokens/s (all layers)",
+        "value": moved * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "ours",
+        "config": {"workload": f"leyline-splice-mla-remap: {L} layers, {S} sequences x "
+                               f"{cfg['seq_len']} tokens, {R} block-aligned directives (spans of "
+                               f"U[{cfg['span_lo']},{cfg['span_hi']}] tokens in whole blocks, "
+                               "stubs of 1-4 blocks) applied by block-table remapping",
+                   "rows_moved_per_step_per_gpu": moved, "downstream_rows": down,
+                   "stub_rows": stub, "layers": L, "amortize_ms": amortize_ms,
+                   "speedup_vs_amortize": amortize_ms / ms,
+                   "parallelism": f"replicas x{world} (independent sequences)",
+                   "l2": "inputs larger than L2 (%.1f GB moved per step); cache and block "
+                         "tables restored before each step, untimed" % (nbytes / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": nbytes / (kms * 1e-3) / 1e9 if kms > 0 else None,
+                     "peak": peak, "unit": "GB/s", "peak_kind": peak_kind, "traffic": None,
+                     "kernel": "remap_data_kernel<MLA> (last round of a step)",
+                     "kernel_ms_last_round": kms, "algorithmic_bytes_per_step": nbytes,
+                     "frac": None},
+        "e2e": None, "clocks": clk, "gpu_launches": launches,
+    }
+    out["roofline"]["frac"] = nbytes / (ms * 1e-3) / 1e9 / peak   # whole step, all rounds
+    out["roofline"]["achieved"] = nbytes / (ms * 1e-3) / 1e9
+    if args.check and rank == 0:
+        import oracle as O
+        restore()
+        splice_step(st, mode=kv.KV_AMORTIZE_REMAP)
+        out["parity_sample"] = check_splice_sample(st, O.get(), final_bt=st["bt"].cpu().numpy())
     return out
 
 
@@ -1396,7 +1469,8 @@ def run_sweep_mla(args, rank, world, local):
 WORKLOADS = {"relocate-mla": run_relocate_mla, "splice-mla-128k": run_splice_mla_128k,
              "relocate-gqa-patch": run_relocate_gqa_patch, "splice-mla-4k": run_splice_mla_4k,
              "relocate-mla-patch": run_relocate_mla_patch, "sweep-mla": run_sweep_mla,
-             "splice-mla-128k-composed": run_splice_mla_128k_composed}
+             "splice-mla-128k-composed": run_splice_mla_128k_composed,
+             "splice-mla-128k-remap": run_splice_mla_128k_remap}
 
 
 def main(argv=None):

@@ -78,8 +78,10 @@ typedef enum {
 
 /* Leyline directive modes (Leyline §2.1). */
 typedef enum {
-    KV_AMORTIZE = 0, /* splice in place, shift + rotate downstream rows */
-    KV_FORGET = 1    /* move nothing; truncate to s_start for a re-prefill */
+    KV_AMORTIZE = 0,      /* splice in place, shift + rotate downstream rows */
+    KV_FORGET = 1,        /* move nothing; truncate to s_start for a re-prefill */
+    KV_AMORTIZE_REMAP = 2 /* AMORTIZE; block-aligned directives move whole blocks by
+                             permuting the block-table row (see kv_splice) */
 } kv_mode;
 
 /* One paged KV pool (device memory, bf16 elements, strides in elements). */
@@ -166,9 +168,20 @@ kv_status kv_relocate(const kv_pool_desc *src, const kv_pool_desc *dst, int32_t 
  * overlap-safe for Δ of either sign.
  * FORGET: moves nothing and sets h_seq_lens[q] = s_start (the caller
  * re-prefills from there); no device work.
+ * AMORTIZE_REMAP: the logical result of AMORTIZE.  A sequence whose directive
+ * is block-aligned (s_start, s_end and |R| multiples of block_size) and
+ * shifts (Δ != 0) keeps its downstream rows in their physical blocks: only
+ * their rotary part is rewritten (R(Δ) in place) and its block-table row is
+ * permuted ON THE DEVICE -- with A = s_start/B, the row becomes [entries
+ * 0..A) [|R|/B blocks for the stub: the span's blocks first, then the row's
+ * entries after the downstream blocks] [the downstream blocks] [the entries
+ * left, in order].  After the call the device row is authoritative; entries
+ * at or beyond the new length remain the sequence's.  Other sequences (and
+ * every sequence when max_blocks > 49152) take the AMORTIZE path and keep
+ * their rows.  d_block_tables is only written in this mode.
  * h_seq_lens is updated when the call returns KV_OK (the data movement itself
  * completes in stream order). */
-kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d_block_tables,
+kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block_tables,
                     int32_t max_blocks, int32_t *h_seq_lens, const int32_t *h_s_start,
                     const int32_t *h_s_end, const int32_t *h_stub_len, const void *d_stub_copy,
                     const void *d_stub_rot, kv_mode mode, void *d_workspace,

@@ -23,7 +23,7 @@ from . import build as _build
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_OUT_OF_RANGE, KV_ERR_CAPACITY = 0, 1, 2, 3
 KV_ERR_WORKSPACE, KV_ERR_TIMEOUT, KV_ERR_CUDA, KV_ERR_UNSUPPORTED = 4, 5, 6, 7
-KV_AMORTIZE, KV_FORGET = 0, 1
+KV_AMORTIZE, KV_FORGET, KV_AMORTIZE_REMAP = 0, 1, 2
 
 LIB_PATH = _build.LIB
 

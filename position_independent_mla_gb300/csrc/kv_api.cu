@@ -462,7 +462,7 @@ kv_status kv_patch(const kv_pool_desc *pool, int32_t num_chunks, int64_t total_t
                          true);
 }
 
-kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d_block_tables,
+kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block_tables,
                     int32_t max_blocks, int32_t *h_seq_lens, const int32_t *h_s_start,
                     const int32_t *h_s_end, const int32_t *h_stub_len, const void *d_stub_copy,
                     const void *d_stub_rot, kv_mode mode, void *d_workspace,
@@ -470,7 +470,8 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d
 {
     t_launches = 0;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    if (!pool_ok(pool) || num_seqs < 0 || (mode != KV_AMORTIZE && mode != KV_FORGET))
+    if (!pool_ok(pool) || num_seqs < 0 ||
+        (mode != KV_AMORTIZE && mode != KV_FORGET && mode != KV_AMORTIZE_REMAP))
         return KV_ERR_INVALID_ARG;
     RowKind kind;
     if (!row_kind(pool, &kind))
@@ -507,6 +508,14 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d
             return KV_ERR_CAPACITY;
     }
 
+    // KV_AMORTIZE_REMAP: block-aligned directives that shift move by
+    // permuting the block-table row; the others take the data-moving path
+    std::vector<char> remap((size_t)num_seqs, 0);
+    if (mode == KV_AMORTIZE_REMAP && max_blocks <= kMaxRemapBlocks)
+        for (int q = 0; q < num_seqs; ++q)
+            remap[q] = h_s_start[q] % B == 0 && h_s_end[q] % B == 0 && h_stub_len[q] % B == 0 &&
+                       h_stub_len[q] != h_s_end[q] - h_s_start[q];
+
     // plan: launches of up to kMaxSeqsPerLaunch sequences each
     const int T = tile_rows(kind);
     const int L = pool->num_layers;
@@ -525,8 +534,8 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d
             S.n_r = h_stub_len[q];
             S.delta = S.n_r - (S.s_end - S.s_start);
             const int64_t down = S.seq_len - S.s_end;
-            S.n_shift = S.delta == 0 ? 0 : (int32_t)((down + T - 1) / T);
-            S.n_stub = (S.n_r + T - 1) / T;
+            S.n_shift = (S.delta == 0 || remap[q]) ? 0 : (int32_t)((down + T - 1) / T);
+            S.n_stub = remap[q] ? 0 : (S.n_r + T - 1) / T;
             S.bt_row = q;
             S.ticket_base = tickets;
             S.flag_base = flags;
@@ -591,6 +600,66 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, const int32_t *d
         KV_CUDA(launch_splice(sp, kind, stream));
         ++t_launches;
     }
+    // remapped sequences: rotary parts in place, stubs into their blocks,
+    // then the permuted block-table rows
+    int64_t remap_stub = 0;
+    std::vector<RemapParams> rplans;
+    {
+        RemapParams rp{};
+        int64_t stub_base = 0;
+        for (int q = 0; q < num_seqs; ++q) {
+            if (remap[q]) {
+                if (rp.num_seqs == kMaxSeqsPerLaunch) {
+                    rplans.push_back(rp);
+                    rp = RemapParams{};
+                }
+                RemapSeq &R = rp.seq[rp.num_seqs++];
+                R.s_start = h_s_start[q];
+                R.s_end = h_s_end[q];
+                R.seq_len = h_seq_lens[q];
+                R.n_r = h_stub_len[q];
+                R.delta = R.n_r - (R.s_end - R.s_start);
+                R.bt_row = q;
+                R.n_down = (int32_t)((R.seq_len - R.s_end + T - 1) / T);
+                R.n_stub = (R.n_r + T - 1) / T;
+                R.tile_base = rp.total_tiles;
+                R.stub_base = stub_base;
+                rp.total_tiles += R.n_down + R.n_stub;
+                ++remap_stub;
+            }
+            stub_base += h_stub_len[q];
+        }
+        if (rp.num_seqs > 0)
+            rplans.push_back(rp);
+    }
+    for (RemapParams &rp : rplans) {
+        TableParams tp{};
+        tp.d_delta = nullptr;
+        for (int i = 0; i < rp.num_seqs; ++i)
+            tp.h_delta[i] = rp.seq[i].delta;
+        tp.units = rp.num_seqs;
+        tp.half = pool->rot_head_dim / 2;
+        tp.head_dim = pool->rot_head_dim;
+        tp.base = pool->rope_base;
+        tp.table = table;
+        KV_CUDA(launch_delta_table(tp, stream));
+        ++t_launches;
+        rp.pool = view_of(pool);
+        rp.block_tables = d_block_tables;
+        rp.max_blocks = max_blocks;
+        rp.stub_copy = static_cast<const char *>(d_stub_copy);
+        rp.stub_rot = static_cast<const char *>(d_stub_rot);
+        rp.total_stub = total_stub;
+        rp.table = table;
+        rp.status = status;
+        if (!marked) {
+            KV_CUDA(mark(t_ev_start, stream));
+            marked = true;
+        }
+        KV_CUDA(launch_remap(rp, kind, stream));
+        t_launches += rp.total_tiles > 0 ? 2 : 1;
+    }
+    (void)remap_stub;
     if (marked)
         KV_CUDA(mark(t_ev_stop, stream));
     for (int q = 0; q < num_seqs; ++q)

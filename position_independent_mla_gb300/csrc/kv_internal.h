@@ -118,6 +118,33 @@ struct ComposedParams {
     int64_t wait_limit_ns;
 };
 
+// Block-aligned splice by remapping (s_start, s_end, n_r multiples of the
+// block size, Δ != 0): downstream rows keep their physical blocks, the
+// block-table row is permuted, only the rotary part is rewritten in place.
+struct RemapSeq {
+    int32_t s_start, s_end, seq_len, n_r;
+    int32_t delta;
+    int32_t bt_row;
+    int32_t n_down;   // tiles of downstream rows (rotated in place)
+    int32_t n_stub;   // tiles of stub rows (written into the stub blocks)
+    int64_t tile_base;
+    int64_t stub_base; // first stub row of this sequence
+};
+
+struct RemapParams {
+    PoolView pool;
+    int32_t *block_tables; // rows are read by the data kernel, rewritten by the commit kernel
+    int32_t max_blocks;
+    const char *stub_copy;
+    const char *stub_rot;
+    int64_t total_stub;
+    const float4 *table; // [num_seqs][head_dim/2]
+    uint32_t *status;
+    int64_t total_tiles;
+    int32_t num_seqs;
+    RemapSeq seq[kMaxSeqsPerLaunch];
+};
+
 struct TableParams {
     const int32_t *d_delta;             // per-unit shifts in device memory, or ...
     int32_t h_delta[kMaxSeqsPerLaunch]; // ... carried in the launch (d_delta == nullptr)

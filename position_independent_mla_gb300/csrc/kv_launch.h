@@ -22,6 +22,10 @@ int patch_tc_launches(RowKind kind); // kernels one launch_patch_tc issues
 cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stream);
 // Composed splice: one ticketed block per tile of p.tiles.
 cudaError_t launch_splice_composed(const ComposedParams &p, RowKind kind, cudaStream_t stream);
+// Block-aligned splice by remapping: the data kernel, then the commit of the
+// permuted block-table rows (dynamic shared memory: max_blocks entries).
+cudaError_t launch_remap(const RemapParams &p, RowKind kind, cudaStream_t stream);
+constexpr int32_t kMaxRemapBlocks = 48 * 1024; // block-table entries one commit block holds
 cudaError_t launch_wait_check(uint32_t *flag, uint32_t *status, int64_t limit_ns,
                               cudaStream_t stream);
 

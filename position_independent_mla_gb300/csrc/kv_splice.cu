@@ -313,6 +313,168 @@ cudaError_t launch_splice_composed(const ComposedParams &p, RowKind kind, cudaSt
 }
 
 // ---------------------------------------------------------------------------
+// Block-aligned splice by remapping the block table.
+//
+// With s_start, s_end and |R| multiples of the block size B and Δ != 0, the
+// downstream rows keep their offsets inside their blocks, so whole blocks can
+// change logical position instead of moving their bytes.  In blocks, with
+// A = s_start / B, Sb span blocks, Nb = |R| / B stub blocks and Db downstream
+// blocks, the row becomes
+//   [old 0..A) [Nb stub blocks] [the Db downstream blocks] [the rest],
+// where the stub blocks are taken first from the span's blocks, then from the
+// row's spare entries past the downstream ones, and "the rest" is what is
+// left of those, in order -- a permutation of the row.  The downstream rows
+// stay where they are physically; only their rotary part is turned by R(Δ)
+// in place (MLA: 256 of 2304 bytes per row and layer).  The stub rows are
+// written into the stub blocks.  Nothing is read that another tile writes,
+// so the tiles need no ordering; the commit kernel rewrites the rows after
+// the data kernel has finished reading them.
+// ---------------------------------------------------------------------------
+
+// Entry j of the permuted row, from the old row.
+__device__ __forceinline__ int32_t remapped_entry(const int32_t *old, int32_t j, int32_t A,
+                                                  int32_t Sb, int32_t Nb, int32_t Db)
+{
+    auto spare = [&](int32_t k) { return k < Sb ? old[A + k] : old[A + Sb + Db + (k - Sb)]; };
+    if (j < A)
+        return old[j];
+    if (j < A + Nb)
+        return spare(j - A);
+    if (j < A + Nb + Db)
+        return old[A + Sb + (j - A - Nb)];
+    return spare(Nb + (j - A - Nb - Db));
+}
+
+template <class G>
+__global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(const __grid_constant__ RemapParams p)
+{
+    __shared__ int64_t s_idx[G::T]; // slot of each row (in place, or the stub's target)
+    __shared__ int64_t s_src[G::T]; // stub tiles: row of the tile's stub rows
+    __shared__ int32_t s_ident[G::T];
+    __shared__ float4 s_cs[G::kHalf];
+
+    const int tid = threadIdx.x;
+    const int64_t t = blockIdx.x;
+    int q = 0;
+    while (q + 1 < p.num_seqs && p.seq[q + 1].tile_base <= t)
+        ++q;
+    const RemapSeq &S = p.seq[q];
+    const int64_t k = t - S.tile_base;
+    const bool down = k < S.n_down;
+    const int32_t *old = p.block_tables + (int64_t)S.bt_row * p.max_blocks;
+    const int32_t B = p.pool.block;
+    const int64_t nb = p.pool.num_blocks;
+    const int32_t A = S.s_start / B, Sb = (S.s_end - S.s_start) / B, Nb = S.n_r / B;
+    const int32_t Db = (int32_t)((S.seq_len - S.s_end + B - 1) / B);
+    if (tid < G::T) {
+        int64_t slot = -1;
+        if (down) {
+            const int64_t pos = S.s_end + k * G::T + tid;
+            if (pos < S.seq_len)
+                slot = slot_of(old, p.max_blocks, B, nb, pos); // stays where it is
+        } else {
+            const int64_t j = (k - S.n_down) * G::T + tid; // stub row
+            if (j < S.n_r) {
+                const int32_t blk = remapped_entry(old, A + (int32_t)(j / B), A, Sb, Nb, Db);
+                slot = (blk >= 0 && blk < nb) ? (int64_t)blk * B + j % B : -1;
+                if (slot < 0)
+                    set_status(p.status, kStatusOutOfRange);
+            }
+        }
+        s_idx[tid] = slot;
+        s_src[tid] = (!down && slot >= 0) ? tid : -1;
+        s_ident[tid] = down ? 0 : 1;
+    }
+    if (down)
+        for (int j = tid; j < G::kHalf; j += kThreads)
+            s_cs[G::cs_index(j)] = p.table[(int64_t)q * G::kHalf + j];
+    __syncthreads();
+
+    const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;
+    PatchAt none{nullptr, 0, nullptr, nullptr};
+    auto layer_rows = [&](int l) {
+        return RowsAt{p.pool.copy + l * p.pool.copy_ls, p.pool.copy_ss,
+                      p.pool.rot + l * p.pool.rot_ls, p.pool.rot_ss};
+    };
+    if (down) {
+        // rotary part only, in place; rows of different layers are
+        // independent, so LB layers of loads are in flight at once
+        constexpr int LB = G::kRotPer >= 8 ? 1 : 8 / G::kRotPer;
+        const int Lc = p.pool.num_layers;
+        for (int l0 = 0; l0 < Lc; l0 += LB) {
+            TileRegs<G> regs[LB];
+#pragma unroll
+            for (int b = 0; b < LB; ++b)
+                if (l0 + b < Lc)
+                    load_tile<G, false>(layer_rows(l0 + b), s_idx, regs[b]);
+#pragma unroll
+            for (int b = 0; b < LB; ++b)
+                if (l0 + b < Lc)
+                    store_tile<G, false, false>(layer_rows(l0 + b), s_idx, regs[b], s_cs, 0,
+                                                s_ident, none);
+        }
+        return;
+    }
+    for (int l = 0; l < p.pool.num_layers; ++l) {
+        const RowsAt pool_l = layer_rows(l);
+        TileRegs<G> regs;
+        {
+            const int64_t j0 = S.stub_base;
+            const RowsAt stub_l{p.stub_copy + (l * p.total_stub + j0 + (k - S.n_down) * G::T) *
+                                                  copy_row_bytes,
+                                copy_row_bytes,
+                                p.stub_rot + (l * p.total_stub + j0 + (k - S.n_down) * G::T) *
+                                                 rot_row_bytes,
+                                rot_row_bytes};
+            // the tile's rows are stub rows 0..T-1 counted from stub_l
+            load_tile<G>(stub_l, s_src, regs);
+            store_tile<G, false>(pool_l, s_idx, regs, s_cs, 0, s_ident, none);
+        }
+    }
+}
+
+// One block per sequence: the whole old row into shared memory, then the
+// permuted row written back over it.
+__global__ void remap_commit_kernel(const __grid_constant__ RemapParams p)
+{
+    extern __shared__ int32_t s_old[];
+    const RemapSeq &S = p.seq[blockIdx.x];
+    int32_t *row = p.block_tables + (int64_t)S.bt_row * p.max_blocks;
+    const int32_t B = p.pool.block;
+    for (int j = threadIdx.x; j < p.max_blocks; j += blockDim.x)
+        s_old[j] = row[j];
+    __syncthreads();
+    const int32_t A = S.s_start / B, Sb = (S.s_end - S.s_start) / B, Nb = S.n_r / B;
+    const int32_t Db = (int32_t)((S.seq_len - S.s_end + B - 1) / B);
+    for (int j = threadIdx.x; j < p.max_blocks; j += blockDim.x)
+        row[j] = remapped_entry(s_old, j, A, Sb, Nb, Db);
+}
+
+cudaError_t launch_remap(const RemapParams &p, RowKind kind, cudaStream_t stream)
+{
+    if (p.num_seqs == 0)
+        return cudaSuccess;
+    if (p.total_tiles > 0) {
+        if (p.total_tiles > 0x7FFFFFFFll)
+            return cudaErrorInvalidConfiguration;
+        if (kind == RowKind::Mla)
+            remap_data_kernel<GeoMla><<<(unsigned)p.total_tiles, kThreads, 0, stream>>>(p);
+        else
+            remap_data_kernel<GeoGqa><<<(unsigned)p.total_tiles, kThreads, 0, stream>>>(p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    const size_t smem = (size_t)p.max_blocks * sizeof(int32_t);
+    cudaError_t e = cudaFuncSetAttribute(remap_commit_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    remap_commit_kernel<<<p.num_seqs, 256, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Failure-path check: the same bounded wait on a flag nothing sets.
 // ---------------------------------------------------------------------------
 

@@ -57,7 +57,8 @@ struct TileRegs {
     uint4 r[G::kRotPer];
 };
 
-template <class G>
+// COPY = false leaves the verbatim part alone (rotary part only).
+template <class G, bool COPY = true>
 __device__ __forceinline__ void load_tile(const RowsAt &at, const int64_t *idx, TileRegs<G> &regs)
 {
     const int tid = threadIdx.x;
@@ -65,7 +66,7 @@ __device__ __forceinline__ void load_tile(const RowsAt &at, const int64_t *idx, 
     for (int k = 0; k < G::kCopyPer; ++k) {
         const int i = tid + k * kThreads;
         regs.c[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (i < G::kCopyItems) {
+        if (COPY && i < G::kCopyItems) {
             const int row = i / G::CV, v = i % G::CV;
             const int64_t s = idx[row];
             if (s >= 0)
@@ -139,7 +140,7 @@ __device__ __forceinline__ void patch_terms(const PatchView &pv, int ch, int l, 
 // rotary vectors turned by the row's cos/sin (a transposed table row at
 // cs + row*cs_row_stride, see Geo::cs_index) unless the row is marked
 // identity.
-template <class G, bool PATCH>
+template <class G, bool PATCH, bool COPY = true>
 __device__ __forceinline__ void store_tile(const RowsAt &at, const int64_t *idx,
                                            const TileRegs<G> &regs, const float4 *cs,
                                            int cs_row_stride, const int32_t *ident,
@@ -153,7 +154,7 @@ __device__ __forceinline__ void store_tile(const RowsAt &at, const int64_t *idx,
 #pragma unroll
     for (int k = 0; k < G::kCopyPer; ++k) {
         const int i = tid + k * kThreads;
-        if (i < G::kCopyItems) {
+        if (COPY && i < G::kCopyItems) {
             const int row = i / G::CV, v = i % G::CV;
             const int64_t s = idx[row];
             if (s >= 0) {

@@ -221,6 +221,23 @@ def random_directives(seed: int, seq_lens, span_lo: int, span_hi: int, stub_lo: 
     return Directives(np.asarray(s0, np.int32), np.asarray(s1, np.int32), np.asarray(nr, np.int32))
 
 
+def random_aligned_directives(seed: int, seq_lens, span_lo: int, span_hi: int, stub_lo: int,
+                              stub_hi: int, block: int = BLOCK) -> Directives:
+    """One block-aligned directive per sequence: a span of U[span_lo, span_hi]
+    tokens rounded down to whole blocks, at a block-aligned uniform offset,
+    replaced by a stub of U[stub_lo, stub_hi] whole blocks."""
+    rng = np.random.default_rng(seed)
+    s0, s1, nr = [], [], []
+    for n in seq_lens:
+        n = int(n)
+        span = block * int(rng.integers(min(span_lo, n) // block, min(span_hi, n) // block + 1))
+        off = block * int(rng.integers(0, (n - span) // block + 1))
+        s0.append(off)
+        s1.append(off + span)
+        nr.append(block * int(rng.integers(stub_lo, stub_hi + 1)))
+    return Directives(np.asarray(s0, np.int32), np.asarray(s1, np.int32), np.asarray(nr, np.int32))
+
+
 def shard(n: int, rank: int, world: int) -> range:
     """Contiguous share of ``n`` independent units for ``rank`` of ``world``."""
     base, extra = divmod(n, world)

@@ -45,6 +45,8 @@ class _Patch(C.Structure):
         ("v_layer_stride", C.c_int64 * 2),
         ("v_chunk_stride", C.c_int64 * 2),
         ("v_col_stride", C.c_int64 * 2),
+        ("u_chunk_tok", C.c_void_p),
+        ("v_chunk", C.c_void_p),
     ]
 
 
@@ -87,6 +89,10 @@ class Patch:
     m: int
     u: Sequence[Optional[np.ndarray]] = field(default_factory=lambda: [None, None])
     v: Sequence[Optional[np.ndarray]] = field(default_factory=lambda: [None, None])
+    # optional per-chunk maps into factors kept per canonical chunk: U row of
+    # the chunk's first token (int64) and V slot of the chunk (int32)
+    u_chunk_tok: Optional[np.ndarray] = None
+    v_chunk: Optional[np.ndarray] = None
 
     def _c(self) -> _Patch:
         p = _Patch()
@@ -107,6 +113,12 @@ class Patch:
             p.v_layer_stride[ch] = v.strides[0] // 4
             p.v_chunk_stride[ch] = v.strides[1] // 4
             p.v_col_stride[ch] = v.strides[2] // 4
+        if self.u_chunk_tok is not None:
+            self.u_chunk_tok = np.ascontiguousarray(self.u_chunk_tok, dtype=np.int64)
+            p.u_chunk_tok = self.u_chunk_tok.ctypes.data
+        if self.v_chunk is not None:
+            self.v_chunk = np.ascontiguousarray(self.v_chunk, dtype=np.int32)
+            p.v_chunk = self.v_chunk.ctypes.data
         return p
 
 

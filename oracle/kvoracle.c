@@ -183,15 +183,24 @@ typedef struct {
  *   U[ch](l, t, r)      = u[ch][l*u_layer_stride[ch] + t*u_tok_stride[ch] + r]
  *   V[ch](l, c, col, r) = v[ch][l*v_layer_stride[ch] + c*v_chunk_stride[ch]
  *                              + col*v_col_stride[ch] + r]
- * t is the token's index in the call's token list (the chunk's first token
- * index plus its offset in the chunk), c the chunk, col the column inside
- * the channel (for the rotated part: head*rot_d + element). */
+ * t is the token's U row and c the chunk's V slot; col is the column inside
+ * the channel (for the rotated part: head*rot_d + element).  By default t is
+ * the token's index in the call's token list (the chunk's first token index
+ * plus its offset in the chunk) and c the chunk's index in the call.  Factors
+ * kept once per canonical chunk and reused by any later call (Kamera's
+ * reorder with one orbit patch, recall of an evicted chunk) are addressed
+ * through the optional per-chunk maps instead:
+ *   u_chunk_tok[c]  U row of chunk c's first token (its tokens follow it),
+ *   v_chunk[c]      V slot of chunk c,
+ * both for both channels; the caller keeps them inside the factor arrays. */
 typedef struct {
     int m;
     const float *u[2];
     int64_t u_layer_stride[2], u_tok_stride[2];
     const float *v[2];
     int64_t v_layer_stride[2], v_chunk_stride[2], v_col_stride[2];
+    const int64_t *u_chunk_tok; /* NULL: the call's token order */
+    const int32_t *v_chunk;     /* NULL: the call's chunk order */
 } kvo_patch;
 
 static int rot_width(const kvo_pool *p) { return p->rot_heads * p->rot_d; }
@@ -230,6 +239,14 @@ static int64_t slot_of(const kvo_pool *p, const int32_t *bt_row, int max_blocks,
 }
 
 /* Σ_r U(l,t,r)·V(l,c,col,r) for one channel, in fp64, r ascending. */
+/* U row of the call's token t (of chunk c) and V slot of chunk c. */
+static int64_t u_row(const kvo_patch *pt, const int32_t *tok_off, int64_t c, int64_t t)
+{
+    return pt->u_chunk_tok ? pt->u_chunk_tok[c] + (t - tok_off[c]) : t;
+}
+
+static int64_t v_slot(const kvo_patch *pt, int64_t c) { return pt->v_chunk ? pt->v_chunk[c] : c; }
+
 static double patch_term(const kvo_patch *pt, int ch, int l, int64_t t, int64_t c, int col)
 {
     const float *u = pt->u[ch] + l * pt->u_layer_stride[ch] + t * pt->u_tok_stride[ch];
@@ -301,7 +318,9 @@ int kvo_relocate(const kvo_pool *src, kvo_pool *dst, int num_chunks, const int32
                 if (has_patch(patch, 0)) {
                     for (int col = 0; col < cd; ++col)
                         dc[col] = kvo_round_bf16(kvo_bf16_to_f64(sc[col]) +
-                                                 patch_term(patch, 0, l, t, c, col));
+                                                 patch_term(patch, 0, l,
+                                                            u_row(patch, tok_off, c, t),
+                                                            v_slot(patch, c), col));
                 } else {
                     memcpy(dc, sc, (size_t)cd * sizeof *dc);
                 }
@@ -315,7 +334,9 @@ int kvo_relocate(const kvo_pool *src, kvo_pool *dst, int num_chunks, const int32
                         }
                         for (int i = 0; i < rd; ++i)
                             dr[h * rd + i] =
-                                kvo_round_bf16(ex[i] + patch_term(patch, 1, l, t, c, h * rd + i));
+                                kvo_round_bf16(ex[i] + patch_term(patch, 1, l,
+                                                                  u_row(patch, tok_off, c, t),
+                                                                  v_slot(patch, c), h * rd + i));
                     } else {
                         kvo_rotate_bf16(sr + h * rd, dr + h * rd, rd, delta[c], src->rope_base);
                     }
@@ -365,7 +386,9 @@ int kvo_patch_apply(kvo_pool *pool, int num_chunks, const int32_t *tok_off,
                         continue;
                     for (int col = 0; col < width[ch]; ++col)
                         row[ch][col] = kvo_round_bf16(kvo_bf16_to_f64(row[ch][col]) +
-                                                      patch_term(patch, ch, l, t, c, col));
+                                                      patch_term(patch, ch, l,
+                                                                 u_row(patch, tok_off, c, t),
+                                                                 v_slot(patch, c), col));
                 }
             }
         }

@@ -38,9 +38,11 @@ MUTANTS = [
      "int64_t d = slot_of(dst, bt, max_blocks, chunk_dst_pos[c] + (tok_off[c + 1] - 1 - t));", 0),
     ("patch-drops-last-rank", "for (int r = 0; r < pt->m; ++r)", "for (int r = 0; r < pt->m - 1; ++r)", 0),
     ("patch-wrong-v-index", "s += (double)u[r] * (double)v[r];", "s += (double)u[r] * (double)v[0];", 0),
-    ("patch-token-index", "patch_term(patch, 0, l, t, c, col)", "patch_term(patch, 0, l, t - tok_off[c], c, col)", 0),
-    ("fused-patch-rounds-twice", "kvo_round_bf16(ex[i] + patch_term(patch, 1, l, t, c, h * rd + i))",
-     "kvo_round_bf16(kvo_bf16_to_f64(kvo_round_bf16(ex[i])) + patch_term(patch, 1, l, t, c, h * rd + i))", 0),
+    ("patch-token-index", "pt->u_chunk_tok[c] + (t - tok_off[c]) : t;", "pt->u_chunk_tok[c] + (t - tok_off[c]) : t - tok_off[c];", 0),
+    ("u-map-drops-offset", "pt->u_chunk_tok[c] + (t - tok_off[c]) :", "pt->u_chunk_tok[c] :", 0),
+    ("v-map-ignored", "pt->v_chunk ? pt->v_chunk[c] : c;", "c;", 0),
+    ("fused-patch-rounds-twice", "kvo_round_bf16(ex[i] + patch_term(patch, 1, l,",
+     "kvo_round_bf16(kvo_bf16_to_f64(kvo_round_bf16(ex[i])) + patch_term(patch, 1, l,", 0),
     ("relocate-ignores-copy-patch", "if (has_patch(patch, 0)) {\n                    for (int col = 0; col < cd; ++col)\n                        dc[col]",
      "if (0) {\n                    for (int col = 0; col < cd; ++col)\n                        dc[col]", 0),
     ("composed-origin-position-zero", "cur[p].written = p;", "cur[p].written = 0;", 0),
@@ -65,6 +67,7 @@ def _pins():
         ("fresh-position", P.test_fresh_position_equivalence),
         ("relocate-brute", lambda o: P.test_relocate_matches_brute_force(o, 2, 8, 16)),
         ("fused-patch", P.test_fused_patch_matches_independent_restatement),
+        ("factor-maps", P.test_factor_maps_reuse_factors_kept_per_chunk),
         ("patch-matmul", P.test_standalone_patch_matches_numpy_matmul),
         ("one-hot-patch", P.test_rank_one_one_hot_patch_touches_one_value),
         ("splice-batch", P.test_splice_batch_of_sequences_with_gqa_heads),

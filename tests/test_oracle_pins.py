@@ -311,6 +311,53 @@ def test_fused_patch_matches_independent_restatement(oracle):
     assert np.array_equal(dst.rot, wr)
 
 
+def _factor_store(wl, seed, widths, m, extra=3, L=2):
+    """Factors kept per canonical chunk: a store with more chunks than the
+    call, the call's chunks mapped into it in a shuffled order.  Returns the
+    store (U, V per channel), the maps and the factors gathered into call
+    order (for a call without maps)."""
+    rng = np.random.default_rng(seed)
+    C = wl.num_chunks
+    lens = np.diff(wl.tok_off)
+    slots = rng.permutation(C + extra)[:C]                # V slot of each call chunk
+    store_len = np.zeros(C + extra, np.int64)
+    store_len[slots] = lens
+    store_off = np.concatenate([[0], np.cumsum(store_len)[:-1]])
+    u_store = [synth.f32_normal((L, int(store_len.sum()) + 5, m), seed + 1 + ch, std=0.4).numpy()
+               for ch in range(2)]
+    v_store = [synth.f32_normal((L, C + extra, widths[ch], m), seed + 3 + ch, std=0.4).numpy()
+               for ch in range(2)]
+    u_map = store_off[slots].astype(np.int64)
+    rows = np.concatenate([np.arange(u_map[c], u_map[c] + lens[c]) for c in range(C)]
+                          ).astype(np.int64)
+    u_call = [np.ascontiguousarray(u[:, rows]) for u in u_store]
+    v_call = [np.ascontiguousarray(v[:, slots]) for v in v_store]
+    return u_store, v_store, u_map, slots.astype(np.int32), u_call, v_call
+
+
+def test_factor_maps_reuse_factors_kept_per_chunk(oracle):
+    # Kamera's reorder / recall: factors stored once per canonical chunk and
+    # addressed per call through the maps give what gathering them into call
+    # order gives, checked against the independent restatement
+    heads, d, cd, m = 2, 8, 16, 4
+    wl, sc, sr, dc, dr = _tiny_relocate_case(27, heads, d, cd)
+    us, vs, umap, vmap, u_call, v_call = _factor_store(wl, 950, (cd, heads * d), m)
+    args = (wl.tok_off, wl.src_slots, wl.chunk_req, wl.chunk_dst_pos, wl.delta, wl.block_tables)
+    src = O.Pool(sc, sr, 4, heads, d, 10000.0)
+    mapped = O.Pool(dc.copy(), dr.copy(), 4, heads, d, 10000.0)
+    assert oracle.relocate(src, mapped, *args, O.Patch(m, us, vs, umap, vmap)) == O.OK
+    wc, wr = ind.relocate(sc, sr, dc, dr, 4, heads, d, 10000.0, *args, patch=(u_call, v_call))
+    assert np.array_equal(mapped.copy, wc) and np.array_equal(mapped.rot, wr)
+    # the standalone patch reads the factors the same way
+    a = O.Pool(wc.copy(), wr.copy(), 4, heads, d, 10000.0)
+    b = O.Pool(wc.copy(), wr.copy(), 4, heads, d, 10000.0)
+    pargs = (wl.tok_off, wl.chunk_req, wl.chunk_dst_pos, wl.block_tables)
+    assert oracle.patch_apply(a, *pargs, O.Patch(m, us, vs, umap, vmap)) == O.OK
+    assert oracle.patch_apply(b, *pargs, O.Patch(m, u_call, v_call)) == O.OK
+    assert np.array_equal(a.copy, b.copy) and np.array_equal(a.rot, b.rot)
+    assert not np.array_equal(a.copy, wc)
+
+
 def test_fused_patch_rounds_once(oracle):
     # a patch fused into the relocation adds to the unrounded rotated value;
     # rounding the rotation first and then the sum differs somewhere

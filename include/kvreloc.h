@@ -106,11 +106,20 @@ typedef struct {
  * unpatched (the same arrays may serve both channels).  fp32:
  *   U(l, t, r)      = u[l*u_layer_stride + t*u_tok_stride + r]
  *   V(l, c, col, r) = v[l*v_layer_stride + c*v_chunk_stride + col*v_col_stride + r]
- * t is the token's index in the call (tok_off[c] + offset in chunk c), col the
- * column inside the channel (rotated part: head*rot_head_dim + i).  Each
- * patched value becomes rnd(x + Σ_r U(l,t,r)·V(l,c,col,r)), x the copied or
- * (fused into kv_relocate) the unrounded rotated value.  An MLA patch over
- * the 576-wide row is one factor pair: u[0] = u[1], v[1] = v[0] + 512*v_col_stride. */
+ * t is the token's U row and c the chunk's V slot; col is the column inside
+ * the channel (rotated part: head*rot_head_dim + i).  Each patched value
+ * becomes rnd(x + Σ_r U(l,t,r)·V(l,c,col,r)), x the copied or (fused into
+ * kv_relocate) the unrounded rotated value.  By default t is the token's
+ * index in the call (tok_off[c] + offset in chunk c) and c the chunk's index
+ * in the call.  Factors kept once per canonical chunk and reused by any
+ * later call (Kamera §3: reorder under one orbit patch, recall of an evicted
+ * chunk) are addressed through the optional device maps instead, for both
+ * channels:
+ *   d_u_chunk_tok[c]  U row of chunk c's first token (its tokens follow it),
+ *   d_v_chunk[c]      V slot of chunk c;
+ * the caller keeps every mapped row and slot inside the factor arrays.  An
+ * MLA patch over the 576-wide row is one factor pair: u[0] = u[1],
+ * v[1] = v[0] + 512*v_col_stride. */
 typedef struct {
     int32_t rank; /* m: 4..64, a multiple of 4 */
     const float *u[2];
@@ -120,6 +129,8 @@ typedef struct {
     int64_t v_layer_stride[2];
     int64_t v_chunk_stride[2];
     int64_t v_col_stride[2];
+    const int64_t *d_u_chunk_tok; /* NULL: the call's token order */
+    const int32_t *d_v_chunk;     /* NULL: the call's chunk order */
 } kv_patch_desc;
 
 /* Bytes of device workspace needed by any call on `pool` that moves at most

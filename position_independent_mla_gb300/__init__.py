@@ -62,6 +62,8 @@ class kv_patch_desc(C.Structure):
         ("v_layer_stride", C.c_int64 * 2),
         ("v_chunk_stride", C.c_int64 * 2),
         ("v_col_stride", C.c_int64 * 2),
+        ("d_u_chunk_tok", C.c_void_p),
+        ("d_v_chunk", C.c_void_p),
     ]
 
 
@@ -167,13 +169,24 @@ def pool_desc(copy: torch.Tensor, rot: torch.Tensor, block_size: int, rot_heads:
 
 
 def patch_desc(rank: int, u: Sequence[Optional[torch.Tensor]],
-               v: Sequence[Optional[torch.Tensor]]) -> kv_patch_desc:
+               v: Sequence[Optional[torch.Tensor]], u_chunk_tok: Optional[torch.Tensor] = None,
+               v_chunk: Optional[torch.Tensor] = None) -> kv_patch_desc:
     """Factors per channel (0 = verbatim part, 1 = rotated part): ``u[ch]``
     fp32 (L, tokens, rank), ``v[ch]`` fp32 (L, chunks, columns, rank), any
-    strides with a unit last stride; None = channel not patched."""
+    strides with a unit last stride; None = channel not patched.  Optional
+    device maps into factors kept per canonical chunk: ``u_chunk_tok`` int64
+    (chunks,) U row of each chunk's first token, ``v_chunk`` int32 (chunks,)
+    V slot of each chunk."""
     d = kv_patch_desc()
     d.rank = rank
-    d._tensors = (list(u), list(v))  # keep the factors alive as long as the descriptor
+    # keep the factors and maps alive as long as the descriptor
+    d._tensors = (list(u), list(v), u_chunk_tok, v_chunk)
+    if u_chunk_tok is not None:
+        assert u_chunk_tok.dtype == torch.int64 and u_chunk_tok.is_contiguous()
+        d.d_u_chunk_tok = u_chunk_tok.data_ptr()
+    if v_chunk is not None:
+        assert v_chunk.dtype == torch.int32 and v_chunk.is_contiguous()
+        d.d_v_chunk = v_chunk.data_ptr()
     for ch in range(2):
         if u[ch] is None or v[ch] is None:
             continue

@@ -99,6 +99,8 @@ kv_status patch_view(const kv_patch_desc *d, PatchView *pv, bool *any)
     if (d->rank < 4 || d->rank > kMaxRank || d->rank % 4 != 0)
         return KV_ERR_INVALID_ARG;
     pv->m = d->rank;
+    pv->u_chunk_tok = d->d_u_chunk_tok;
+    pv->v_chunk = d->d_v_chunk;
     for (int ch = 0; ch < 2; ++ch) {
         if (!d->u[ch] || !d->v[ch])
             continue;

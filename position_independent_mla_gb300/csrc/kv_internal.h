@@ -35,6 +35,8 @@ struct PatchView {
     int64_t u_ls[2], u_ts[2];
     const float *v[2];
     int64_t v_ls[2], v_cs[2], v_cols[2];
+    const int64_t *u_chunk_tok; // per chunk: U row of its first token (nullptr: call order)
+    const int32_t *v_chunk;     // per chunk: V slot (nullptr: call order)
 };
 
 // kv_relocate (in_place = 0) and kv_patch (in_place = 1: rows are read from

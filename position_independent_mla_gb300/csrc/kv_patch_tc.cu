@@ -296,6 +296,8 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
         return; // in place and nothing to add: the rows stay as they are
     const int64_t t0 = p.tok_off[c];
     const int64_t n = max((int64_t)0, (int64_t)p.tok_off[c + 1] - t0);
+    // U row of the chunk's first token: call order, or the caller's map
+    const int64_t u0 = p.patch.u_chunk_tok ? p.patch.u_chunk_tok[c] : t0;
     const int32_t req = p.chunk_req[c];
     const bool req_ok = req >= 0 && req < p.num_reqs;
     const int32_t *bt = p.block_tables + (int64_t)(req_ok ? req : 0) * p.max_blocks;
@@ -316,8 +318,9 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
 
     // --- once per block: V's slice as the B operand, cos/sin, barriers, TMEM
     if (patched) {
+        const int64_t vslot = p.patch.v_chunk ? p.patch.v_chunk[c] : c;
         const float *vb = p.patch.v[ch] + (int64_t)l * p.patch.v_ls[ch] +
-                          (int64_t)c * p.patch.v_cs[ch] + (int64_t)col0 * p.patch.v_cols[ch];
+                          vslot * p.patch.v_cs[ch] + (int64_t)col0 * p.patch.v_cols[ch];
         for (int i = tid; i < G::NB * 2; i += G::NT) {
             const int nn = i >> 1, k0 = (i & 1) * 8;
             float v[8];
@@ -406,7 +409,7 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
                 float u[8];
                 if (i < n) {
                     load_factor8(p.patch.u[ch] + (int64_t)l * p.patch.u_ls[ch] +
-                                     (t0 + i) * p.patch.u_ts[ch],
+                                     (u0 + i) * p.patch.u_ts[ch],
                                  k0, m, u);
                 } else {
 #pragma unroll

@@ -55,8 +55,9 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const
 {
     __shared__ int64_t s_src[G::T];
     __shared__ int64_t s_dst[G::T];
-    __shared__ int64_t s_tok[G::T];
-    __shared__ int32_t s_chunk[G::T];
+    __shared__ int64_t s_tok[G::T];   // U row of the row's token (patch)
+    __shared__ int32_t s_chunk[G::T]; // chunk of the row (δ-table row)
+    __shared__ int32_t s_vslot[G::T]; // V slot of the row's chunk (patch)
     __shared__ int32_t s_ident[G::T];
     __shared__ float4 s_cs[G::T][G::kCsRow];
 
@@ -104,8 +105,13 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const
         }
         s_src[tid] = src;
         s_dst[tid] = dst;
-        s_tok[tid] = t;
+        // the patch's U row and V slot: call order, or the caller's maps
+        const bool live = t < p.total_tokens;
+        s_tok[tid] = (live && p.patch.u_chunk_tok)
+                         ? p.patch.u_chunk_tok[c] + (t - p.tok_off[c])
+                         : t;
         s_chunk[tid] = c;
+        s_vslot[tid] = (live && p.patch.v_chunk) ? p.patch.v_chunk[c] : c;
         s_ident[tid] = ident;
     }
     __syncthreads();
@@ -119,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const
         __syncthreads();
     }
 
-    PatchAt pa{&p.patch, 0, s_tok, s_chunk};
+    PatchAt pa{&p.patch, 0, s_tok, s_vslot};
     for (int l = 0; l < p.src.num_layers; ++l) {
         const RowsAt from{p.src.copy + l * p.src.copy_ls, p.src.copy_ss,
                           p.src.rot + l * p.src.rot_ls, p.src.rot_ss};

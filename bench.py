@@ -1215,6 +1215,224 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------------------
+# Workload: Kamera sliding window (GQA): survival by remapping + recall
+# ---------------------------------------------------------------------------
+
+WINDOW_GQA = dict(layers=32, num_reqs=16, window=64, chunk_len=576, slide=8, n_canon=256,
+                  rank=16, std=0.02, base=500000.0)
+# A small case of the same kernels (~1.3 GB).
+WINDOW_GQA_SMALL = dict(WINDOW_GQA, num_reqs=1, window=16, slide=4, n_canon=32)
+
+
+def build_window_gqa(rank: int, cfg):
+    """A canonical store (chunks prefilled alone at position 0, GQA K and V,
+    one rank-m patch per canonical chunk and channel) and a per-request
+    window of `window` chunks filled from it."""
+    import position_independent_mla_gb300 as kv
+
+    c = cfg
+    L, R, W, cl, m, W1 = c["layers"], c["num_reqs"], c["window"], c["chunk_len"], c["rank"], 1024
+    nc = c["n_canon"]
+    reg_k = torch.empty((L, nc * cl, W1), dtype=torch.bfloat16, device="cuda")
+    reg_v = torch.empty_like(reg_k)
+    fill_normal_(reg_k, 7007 + 100 * rank)
+    fill_normal_(reg_v, 7008 + 100 * rank)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7009 + 100 * rank)
+    u = [torch.randn((L, nc * cl, m), generator=g, device="cuda").mul_(c["std"]) for _ in range(2)]
+    v = [torch.randn((L, nc, W1, m), generator=g, device="cuda").mul_(c["std"]) for _ in range(2)]
+    mb = W * cl // 64
+    win_k = torch.zeros((L, R * mb * 64, W1), dtype=torch.bfloat16, device="cuda")
+    win_v = torch.zeros_like(win_k)
+    rng = np.random.default_rng(7010 + 100 * rank)
+    bt0 = rng.permutation(R * mb).astype(np.int32).reshape(R, mb)
+    ids = np.array([[(r * W + j) % nc for j in range(W)] for r in range(R)], np.int64)
+    st = dict(cfg=c, L=L, R=R, W=W, cl=cl, m=m, mb=mb, ids=ids, bt0=bt0, u=u, v=v,
+              reg_k=reg_k, reg_v=reg_v, win_k=win_k, win_v=win_v,
+              sd=kv.pool_desc(reg_v, reg_k, 64, 8, c["base"]),
+              wd=kv.pool_desc(win_v, win_k, 64, 8, c["base"]),
+              bt=torch.from_numpy(bt0.copy()).cuda())
+    st["ws"] = kv.workspace(st["wd"], R * W * cl, R * W)
+    return st
+
+
+def window_recall_args(st, chunks, slot0):
+    """kv_relocate arguments bringing canonical chunks[r][j] of each request r
+    to window positions (slot0 + j) * chunk_len, with their stored patches."""
+    import position_independent_mla_gb300 as kv
+
+    R, cl = st["R"], st["cl"]
+    n = chunks.shape[1]
+    ids = chunks.reshape(-1)
+    pos = np.tile((slot0 + np.arange(n)) * cl, R).astype(np.int32)
+    args = dict(
+        tok_off=(np.arange(R * n + 1) * cl).astype(np.int32),
+        src_slots=(ids[:, None] * cl + np.arange(cl)[None, :]).reshape(-1).astype(np.int32),
+        chunk_req=np.repeat(np.arange(R), n).astype(np.int32), chunk_dst_pos=pos,
+        delta=pos.copy())                                  # canonical chunks sit at position 0
+    dev = {k: torch.from_numpy(v_).cuda() for k, v_ in args.items()}
+    pd = kv.patch_desc(st["m"], st["u"], st["v"], torch.from_numpy(ids * cl).cuda(),
+                       torch.from_numpy(ids.astype(np.int32)).cuda())
+    return dict(host=args, dev=dev, pd=pd, n=R * n)
+
+
+def window_relocate(st, ra):
+    import position_independent_mla_gb300 as kv
+
+    d, cl = ra["dev"], st["cl"]
+    kv.kv_relocate(st["sd"], st["wd"], ra["n"], ra["n"] * cl, d["tok_off"], d["src_slots"],
+                   d["chunk_req"], d["chunk_dst_pos"], d["delta"], st["bt"], st["R"], st["mb"],
+                   ra["pd"], st["ws"])
+    return kv.kv_last_launch_count()
+
+
+def window_slide(st, mode):
+    import position_independent_mla_gb300 as kv
+
+    R, W, cl, sl = st["R"], st["W"], st["cl"], st["cfg"]["slide"]
+    lens = torch.full((R,), W * cl, dtype=torch.int32)
+    z = torch.zeros(R, dtype=torch.int32)
+    kv.kv_splice(st["wd"], R, st["bt"], st["mb"], lens, z, torch.full((R,), sl * cl,
+                 dtype=torch.int32), z, None, None, mode, st["ws"])
+    return kv.kv_last_launch_count()
+
+
+def check_window_sample(st, recall, orc, n_rows: int = 120, seed: int = 17) -> dict:
+    """After one step from a fresh window: survivors are their first placement
+    turned by R(-slide * chunk_len) (rotary part) and unchanged otherwise;
+    recalled chunks are a fresh relocation + stored patch at the window's end.
+    Each sampled row is rebuilt by the oracle on a one-token problem."""
+    import oracle as O
+
+    c, L, cl, W, sl = st["cfg"], st["L"], st["cl"], st["W"], st["cfg"]["slide"]
+    rng = np.random.default_rng(seed)
+    bt = st["bt"].cpu().numpy()
+    out = {"v_beyond": 0, "k_beyond": 0, "exact": 0, "one_ulp": 0, "values": 0}
+    for _ in range(n_rows):
+        r, p, l = int(rng.integers(st["R"])), int(rng.integers(W * cl)), int(rng.integers(L))
+        j, i = p // cl, p % cl
+        survivor = j < W - sl
+        cid = int(st["ids"][r, j + sl] if survivor else st["ids"][r, j - (W - sl)])
+        p0 = p + sl * cl if survivor else p               # position of its relocation
+        row = cid * cl + i
+        sv = np.zeros((1, 64, 1024), np.uint16)
+        sk = np.zeros((1, 64, 1024), np.uint16)
+        sv[0, 0] = synth.bits(st["reg_v"][l, row].cpu())
+        sk[0, 0] = synth.bits(st["reg_k"][l, row].cpu())
+        src = O.Pool(sv, sk, 64, 8, 128, c["base"])
+        dst = O.Pool(np.zeros_like(sv), np.zeros_like(sk), 64, 8, 128, c["base"])
+        u = [x[l, row].cpu().numpy().reshape(1, 1, -1) for x in st["u"]]
+        v = [x[l, cid].cpu().numpy().reshape(1, 1, 1024, -1) for x in st["v"]]
+        # canonical chunks were prefilled from position 0: δ is the chunk's start
+        assert orc.relocate(src, dst, [0, 1], [0], [0], [0], [p0 - i], [[0]],
+                            O.Patch(st["m"], u, v)) == O.OK
+        want_v, want_k = dst.copy[0, 0], dst.rot[0, 0]
+        if survivor:
+            want_k = np.concatenate([orc.rotate_bf16(want_k[h * 128:(h + 1) * 128], -sl * cl,
+                                                     c["base"]) for h in range(8)])
+        slot = int(bt[r, p // 64]) * 64 + p % 64
+        got_v = synth.bits(st["win_v"][l, slot].cpu())
+        got_k = synth.bits(st["win_k"][l, slot].cpu())
+        for got, want, key in ((got_v, want_v, "v_beyond"), (got_k, want_k, "k_beyond")):
+            rs = ulp_stats(got, want)
+            out[key] += rs["beyond"]
+            out["exact"] += rs["exact"]
+            out["one_ulp"] += rs["one_ulp"]
+            out["values"] += rs["values"]
+    out["rows"] = n_rows
+    return out
+
+
+def run_window_gqa(args, rank, world, local):
+    """Kamera's sliding window, GQA, in steady state: each step evicts the
+    `slide` oldest chunks of every request's window (survival: the survivors'
+    K turned by R(-slide * chunk_len), no patch, by block-table remapping) and
+    recalls them at the window's end from the canonical store with their
+    stored rank-16 patches (relocation + patch through the factor maps), so
+    the window cycles.  Timed against the same step with a data-moving slide."""
+    import position_independent_mla_gb300 as kv
+
+    cfg = WINDOW_GQA_SMALL if args.small else WINDOW_GQA
+    st = build_window_gqa(rank, cfg)
+    L, R, W, cl, sl, m = st["L"], st["R"], st["W"], st["cl"], cfg["slide"], st["m"]
+    window_relocate(st, window_recall_args(st, st["ids"], 0))      # fill, untimed
+    phases = W // sl
+    recalls = [window_recall_args(st, np.roll(st["ids"], -k * sl, axis=1)[:, W - sl:], W - sl)
+               for k in range(1, phases + 1)]
+    out_check = None
+    if args.check and rank == 0:
+        import oracle as O
+        window_slide(st, kv.KV_AMORTIZE_REMAP)
+        window_relocate(st, recalls[0])
+        out_check = check_window_sample(st, recalls[0], O.get())
+        st["bt"].copy_(torch.from_numpy(st["bt0"]))                # start over
+        window_relocate(st, window_recall_args(st, st["ids"], 0))
+    step_no = [0]
+
+    def step(mode):
+        def call():
+            n = window_slide(st, mode)
+            n += window_relocate(st, recalls[step_no[0] % phases])
+            step_no[0] += 1
+            return n
+        return call
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    K, Wu = args.steps, args.warmup
+    ms, _, launches = _timed(step(kv.KV_AMORTIZE_REMAP), K, Wu)
+    amortize_ms, _, _ = _timed(step(kv.KV_AMORTIZE), K, Wu)
+    # the two halves of a step, each between events on the stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for k in range(K):
+        ev[k][0].record()
+        window_slide(st, kv.KV_AMORTIZE_REMAP)
+        ev[k][1].record()
+        window_relocate(st, recalls[step_no[0] % phases])
+        step_no[0] += 1
+        ev[k][2].record()
+    torch.cuda.synchronize()
+    slide_ms = float(np.median([e[0].elapsed_time(e[1]) for e in ev]))
+    recall_ms = float(np.median([e[1].elapsed_time(e[2]) for e in ev]))
+    barrier(world)
+    clk = clocks.stop()
+    assert kv.kv_get_device_status(st["ws"]) == kv.KV_OK
+    ms = max_over_ranks(ms, world)
+    surv, rec = R * (W - sl) * cl, R * sl * cl
+    nbytes = (surv * L * 2 * 2048 + rec * (L * (2 * 4096 + 2 * m * 4) + 4) +
+              R * sl * L * 2 * 1024 * m * 4)
+    peak, peak_kind = hbm_peak()
+    out = {
+        "metric": "relocated KV tokens/s (all layers)",
+        "value": (surv + rec) * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": Wu, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "impl": "ours",
+        "config": {"workload": f"kamera-window-gqa: {L} layers, K and V of 8 x 128, {R} "
+                               f"requests x a window of {W} chunks of {cl} tokens; each step "
+                               f"evicts the {sl} oldest chunks (survivors re-rotated by block-"
+                               f"table remapping) and recalls them at the end from the canonical "
+                               f"store with their stored rank-{m} patches",
+                   "survivor_rows": surv, "recalled_rows": rec, "layers": L,
+                   "amortize_slide_ms": amortize_ms, "speedup_vs_amortize": amortize_ms / ms,
+                   "slide_ms": slide_ms, "recall_ms": recall_ms,
+                   "slide_gbs": surv * L * 2 * 2048 / (slide_ms * 1e-3) / 1e9,
+                   "parallelism": f"replicas x{world} (independent requests)",
+                   "l2": "inputs larger than L2 (%.1f GB moved per step)" % (nbytes / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": nbytes / (ms * 1e-3) / 1e9 / peak,
+                     "peak_kind": peak_kind, "traffic": None,
+                     "kernel": "remap_data_kernel<GQA> + patch_tc_kernel (whole step)",
+                     "algorithmic_bytes_per_step": nbytes},
+        "e2e": None, "clocks": clk, "gpu_launches": launches,
+    }
+    if out_check is not None:
+        out["parity_sample"] = out_check
+    return out
+
+
+# ---------------------------------------------------------------------------
 # Workload: MLA sweep over chunk length x δ (relocate; splice with Δ = δ; patch)
 # ---------------------------------------------------------------------------
 
@@ -1470,7 +1688,8 @@ WORKLOADS = {"relocate-mla": run_relocate_mla, "splice-mla-128k": run_splice_mla
              "relocate-gqa-patch": run_relocate_gqa_patch, "splice-mla-4k": run_splice_mla_4k,
              "relocate-mla-patch": run_relocate_mla_patch, "sweep-mla": run_sweep_mla,
              "splice-mla-128k-composed": run_splice_mla_128k_composed,
-             "splice-mla-128k-remap": run_splice_mla_128k_remap}
+             "splice-mla-128k-remap": run_splice_mla_128k_remap,
+             "window-gqa": run_window_gqa}
 
 
 def main(argv=None):

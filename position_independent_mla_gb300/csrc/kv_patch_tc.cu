@@ -154,63 +154,6 @@ __device__ __forceinline__ void load_factor8(const float *row, int k0, int m, fl
     }
 }
 
-// Two fp32 lanes in one 64-bit register, for the packed f32x2 arithmetic.
-typedef unsigned long long f2;
-
-// bf16 pair (low half = first element) -> fp32 pair, exact.
-__device__ __forceinline__ f2 f2_of_bf16x2(uint32_t w)
-{
-    f2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xFFFF0000u));
-    return r;
-}
-
-__device__ __forceinline__ f2 f2_of_bits(uint32_t lo, uint32_t hi)
-{
-    f2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-    return r;
-}
-
-__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c)
-{
-    f2 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-__device__ __forceinline__ f2 f2_mul(f2 a, f2 b)
-{
-    f2 d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-__device__ __forceinline__ f2 f2_add(f2 a, f2 b)
-{
-    f2 d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// fp32 pair -> bf16 pair, each rounded to nearest even (NaN stays NaN).
-__device__ __forceinline__ uint32_t bf16x2_rne(f2 v)
-{
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    uint32_t d;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-    return d;
-}
-
-// True when either lane is NaN.
-__device__ __forceinline__ bool f2_has_nan(f2 v)
-{
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return lo != lo || hi != hi;
-}
-
 // Bulk (non-tensor) TMA copies of whole rows between global and shared
 // memory; addresses and sizes are multiples of 16 bytes.
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes)

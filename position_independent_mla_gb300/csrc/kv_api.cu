@@ -65,6 +65,14 @@ bool row_kind(const kv_pool_desc *p, RowKind *kind)
         *kind = RowKind::Gqa;
         return true;
     }
+    if (p->copy_dim == 512 && p->rot_heads == 4 && p->rot_head_dim == 128) {
+        *kind = RowKind::Gqa4;
+        return true;
+    }
+    if (p->copy_dim == 4096 && p->rot_heads == 32 && p->rot_head_dim == 128) {
+        *kind = RowKind::Mha;
+        return true;
+    }
     return false;
 }
 

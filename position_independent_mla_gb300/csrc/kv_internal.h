@@ -13,6 +13,8 @@ constexpr int kMaxRank = 64;          // largest patch rank
 constexpr int kHeaderBytes = 256;     // workspace header: status word, ticket counter
 constexpr int kTileMla = 32;          // rows per tile for MLA rows (576 bf16)
 constexpr int kTileGqa = 16;          // rows per tile for 8 x 128 GQA rows
+constexpr int kTileGqa4 = 32;         // rows per tile for 4 x 128 GQA rows
+constexpr int kTileMha = 4;           // rows per tile for 32 x 128 MHA rows
 
 // Device status codes (same values as kv_status).
 enum : uint32_t { kStatusOk = 0, kStatusOutOfRange = 2, kStatusTimeout = 5 };

@@ -7,8 +7,10 @@ namespace kvr {
 
 // Row shapes with a compiled kernel.
 enum class RowKind {
-    Mla, // verbatim 512 + rotary 1 x 64 (c_KV + k_pe)
-    Gqa  // verbatim 1024 + rotary 8 x 128 (V + K)
+    Mla,  // verbatim 512 + rotary 1 x 64 (c_KV + k_pe)
+    Gqa,  // verbatim 1024 + rotary 8 x 128 (V + K, 8 KV heads)
+    Gqa4, // verbatim 512 + rotary 4 x 128 (V + K, 4 KV heads)
+    Mha   // verbatim 4096 + rotary 32 x 128 (V + K, 32 heads)
 };
 
 cudaError_t launch_delta_table(const TableParams &p, cudaStream_t stream);
@@ -30,6 +32,19 @@ cudaError_t launch_wait_check(uint32_t *flag, uint32_t *status, int64_t limit_ns
                               cudaStream_t stream);
 
 // Rows per tile of each kind (splice workspace sizing).
-inline int tile_rows(RowKind kind) { return kind == RowKind::Mla ? kTileMla : kTileGqa; }
+inline int tile_rows(RowKind kind)
+{
+    switch (kind) {
+    case RowKind::Mla:
+        return kTileMla;
+    case RowKind::Gqa:
+        return kTileGqa;
+    case RowKind::Gqa4:
+        return kTileGqa4;
+    case RowKind::Mha:
+        return kTileMha;
+    }
+    return kTileGqa;
+}
 
 } // namespace kvr

@@ -542,14 +542,17 @@ bool patch_tc_supported(const RelocParams &p, RowKind kind)
     return p.patched && p.patch.m <= tc::KP && p.src.num_layers <= 65535;
 }
 
-int patch_tc_launches(RowKind kind) { return kind == RowKind::Gqa ? 1 : 2; }
+int patch_tc_launches(RowKind kind) { return kind == RowKind::Mla ? 2 : 1; }
 
 cudaError_t launch_patch_tc(const RelocParams &p, RowKind kind, cudaStream_t stream)
 {
     if (p.num_chunks == 0)
         return cudaSuccess;
-    if (kind == RowKind::Gqa) // both channels 1024 wide: 4 slices of two heads
-        return tc::launch_geo<tc::TcGeo<256, 128>>(p, tc::TcLaunch{0, 2, 4}, stream);
+    if (kind != RowKind::Mla) {
+        // K and V rows of H heads of 128: H / 2 slices of two heads per channel
+        const int32_t slices = kind == RowKind::Gqa ? 4 : kind == RowKind::Gqa4 ? 2 : 16;
+        return tc::launch_geo<tc::TcGeo<256, 128>>(p, tc::TcLaunch{0, 2, slices}, stream);
+    }
     // MLA: the 512-wide latent as 2 slices of 256, the 64-wide k_pe as one slice
     cudaError_t e = tc::launch_geo<tc::TcGeo<256, 128>>(p, tc::TcLaunch{0, 1, 2}, stream);
     if (e != cudaSuccess)

@@ -155,13 +155,9 @@ static cudaError_t launch_reloc_shape(const RelocParams &p, cudaStream_t stream)
 
 cudaError_t launch_relocate(const RelocParams &p, RowKind kind, cudaStream_t stream)
 {
-    switch (kind) {
-    case RowKind::Mla:
-        return launch_reloc_shape<GeoMla>(p, stream);
-    case RowKind::Gqa:
-        return launch_reloc_shape<GeoGqa>(p, stream);
-    }
-    return cudaErrorInvalidValue;
+    return with_geo(kind, [&](auto g) {
+        return launch_reloc_shape<typename decltype(g)::type>(p, stream);
+    });
 }
 
 } // namespace kvr

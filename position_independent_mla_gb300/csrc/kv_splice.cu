@@ -183,11 +183,10 @@ cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stre
     if (p.total_tickets > 0x7FFFFFFFll)
         return cudaErrorInvalidConfiguration;
     const unsigned blocks = (unsigned)p.total_tickets;
-    if (kind == RowKind::Mla)
-        splice_kernel<GeoMla><<<blocks, kThreads, 0, stream>>>(p);
-    else
-        splice_kernel<GeoGqa><<<blocks, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return with_geo(kind, [&](auto g) {
+        splice_kernel<typename decltype(g)::type><<<blocks, kThreads, 0, stream>>>(p);
+        return cudaGetLastError();
+    });
 }
 
 // ---------------------------------------------------------------------------
@@ -305,11 +304,10 @@ cudaError_t launch_splice_composed(const ComposedParams &p, RowKind kind, cudaSt
     if (p.num_tiles > 0x7FFFFFFFll)
         return cudaErrorInvalidConfiguration;
     const unsigned blocks = (unsigned)p.num_tiles;
-    if (kind == RowKind::Mla)
-        splice_composed_kernel<GeoMla><<<blocks, kThreads, 0, stream>>>(p);
-    else
-        splice_composed_kernel<GeoGqa><<<blocks, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return with_geo(kind, [&](auto g) {
+        splice_composed_kernel<typename decltype(g)::type><<<blocks, kThreads, 0, stream>>>(p);
+        return cudaGetLastError();
+    });
 }
 
 // ---------------------------------------------------------------------------
@@ -457,11 +455,11 @@ cudaError_t launch_remap(const RemapParams &p, RowKind kind, cudaStream_t stream
     if (p.total_tiles > 0) {
         if (p.total_tiles > 0x7FFFFFFFll)
             return cudaErrorInvalidConfiguration;
-        if (kind == RowKind::Mla)
-            remap_data_kernel<GeoMla><<<(unsigned)p.total_tiles, kThreads, 0, stream>>>(p);
-        else
-            remap_data_kernel<GeoGqa><<<(unsigned)p.total_tiles, kThreads, 0, stream>>>(p);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = with_geo(kind, [&](auto g) {
+            remap_data_kernel<typename decltype(g)::type>
+                <<<(unsigned)p.total_tiles, kThreads, 0, stream>>>(p);
+            return cudaGetLastError();
+        });
         if (e != cudaSuccess)
             return e;
     }

@@ -11,6 +11,7 @@
 #pragma once
 
 #include "kv_device.cuh"
+#include "kv_launch.h"
 
 namespace kvr {
 
@@ -40,6 +41,32 @@ struct Geo {
 using GeoMla = Geo<kTileMla, 64, 1, 4, 4>;
 // GQA rows: V 8x128 + K 8x128 (Llama-3-8B shape).
 using GeoGqa = Geo<kTileGqa, 128, 8, 8, 2>;
+// GQA rows with 4 KV heads: V 4x128 + K 4x128 (Qwen2.5-7B shape).
+using GeoGqa4 = Geo<kTileGqa4, 64, 4, 8, 2>;
+// MHA rows: V 32x128 + K 32x128 (Llama-2-7B shape).
+using GeoMha = Geo<kTileMha, 512, 32, 8, 2>;
+
+template <class G>
+struct GeoTag {
+    using type = G;
+};
+
+// Call f(GeoTag<G>{}) with the tile geometry of `kind`.
+template <class F>
+cudaError_t with_geo(RowKind kind, F &&f)
+{
+    switch (kind) {
+    case RowKind::Mla:
+        return f(GeoTag<GeoMla>{});
+    case RowKind::Gqa:
+        return f(GeoTag<GeoGqa>{});
+    case RowKind::Gqa4:
+        return f(GeoTag<GeoGqa4>{});
+    case RowKind::Mha:
+        return f(GeoTag<GeoMha>{});
+    }
+    return cudaErrorInvalidValue;
+}
 
 // Where the rows of a tile live for one layer: row r's verbatim part starts
 // at cbase + idx[r]*cstride, its rotary part at rbase + idx[r]*rstride

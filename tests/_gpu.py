@@ -19,6 +19,8 @@ SHAPES = {
     # name: (copy_dim, rot_heads, rot_head_dim, rope_base)
     "mla": (512, 1, 64, 10000.0),
     "gqa": (1024, 8, 128, 500000.0),
+    "gqa4": (512, 4, 128, 1000000.0),
+    "mha": (4096, 32, 128, 10000.0),
 }
 
 

@@ -32,6 +32,7 @@ class _Pool(C.Structure):
         ("rope_base", C.c_double),
         ("copy", C.c_void_p),
         ("rot", C.c_void_p),
+        ("pair_convention", C.c_int),
     ]
 
 
@@ -64,6 +65,7 @@ class Pool:
     rot_heads: int
     rot_d: int
     rope_base: float
+    pair_convention: int = 0   # 0: rotate-half pairs (x[j], x[j+d/2]); 1: interleaved
 
     def __post_init__(self):
         assert self.copy.dtype == np.uint16 and self.rot.dtype == np.uint16
@@ -74,7 +76,8 @@ class Pool:
     def _c(self) -> _Pool:
         L, S, cd = self.copy.shape
         return _Pool(L, S, self.block_size, cd, self.rot_heads, self.rot_d,
-                     float(self.rope_base), self.copy.ctypes.data, self.rot.ctypes.data)
+                     float(self.rope_base), self.copy.ctypes.data, self.rot.ctypes.data,
+                     int(self.pair_convention))
 
 
 @dataclass
@@ -153,6 +156,8 @@ class Oracle:
         lib.kvo_theta.argtypes = [dbl, i32, i32]
         lib.kvo_rotate_f64.argtypes = [vp, vp, i32, i64, dbl]
         lib.kvo_rotate_bf16.argtypes = [vp, vp, i32, i64, dbl]
+        lib.kvo_rotate_bf16_il.argtypes = [vp, vp, i32, i64, dbl]
+        lib.kvo_rotate_f64_il.argtypes = [vp, vp, i32, i64, dbl]
         lib.kvo_relocate.restype = i32
         lib.kvo_relocate.argtypes = [C.POINTER(_Pool), C.POINTER(_Pool), i32, vp, vp, vp, vp, vp,
                                      vp, i32, i32, C.POINTER(_Patch)]
@@ -192,10 +197,11 @@ class Oracle:
         self._lib.kvo_rotate_f64(x.ctypes.data, y.ctypes.data, x.shape[-1], int(delta), base)
         return y
 
-    def rotate_bf16(self, x, delta: int, base: float) -> np.ndarray:
+    def rotate_bf16(self, x, delta: int, base: float, interleaved: bool = False) -> np.ndarray:
         x = np.ascontiguousarray(np.asarray(x, dtype=np.uint16))
         y = np.empty_like(x)
-        self._lib.kvo_rotate_bf16(x.ctypes.data, y.ctypes.data, x.shape[-1], int(delta), base)
+        fn = self._lib.kvo_rotate_bf16_il if interleaved else self._lib.kvo_rotate_bf16
+        fn(x.ctypes.data, y.ctypes.data, x.shape[-1], int(delta), base)
         return y
 
     # -- the three operations ------------------------------------------------

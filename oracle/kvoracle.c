@@ -139,26 +139,56 @@ void kvo_rotate_f64(const double *x, double *y, int d, int64_t delta, double bas
     }
 }
 
-/* y_exact = R(δ)·x in fp64 for a bf16 vector x (not rounded). */
-static void rotate_bf16_exact(const uint16_t *x, double *y, int d, int64_t delta, double base)
+/* The same rotation with the interleaved pairing that some models store
+ * k_pe in: pair j is (x[2j], x[2j+1]), with the same θ_j. */
+void kvo_rotate_f64_il(const double *x, double *y, int d, int64_t delta, double base)
+{
+    for (int j = 0; j < d / 2; ++j) {
+        double a = (double)delta * kvo_theta(base, j, d);
+        double c = cos(a), s = sin(a);
+        double even = x[2 * j], odd = x[2 * j + 1];
+        y[2 * j] = even * c - odd * s;
+        y[2 * j + 1] = even * s + odd * c;
+    }
+}
+
+/* y_exact = R(δ)·x in fp64 for a bf16 vector x (not rounded); `il` selects
+ * the interleaved pairing. */
+static void rotate_bf16_exact(const uint16_t *x, double *y, int d, int64_t delta, double base,
+                              int il)
 {
     for (int i = 0; i < d; ++i)
         y[i] = kvo_bf16_to_f64(x[i]);
-    kvo_rotate_f64(y, y, d, delta, base);
+    if (il)
+        kvo_rotate_f64_il(y, y, d, delta, base);
+    else
+        kvo_rotate_f64(y, y, d, delta, base);
 }
 
-/* y = rnd(R(δ)·x) on bf16 vectors.  R(0) is the identity, bit for bit
- * (this also fixes the sign of zeros).  x and y may alias. */
-void kvo_rotate_bf16(const uint16_t *x, uint16_t *y, int d, int64_t delta, double base)
+static void rotate_bf16_pairs(const uint16_t *x, uint16_t *y, int d, int64_t delta, double base,
+                              int il)
 {
     if (delta == 0) {
         memmove(y, x, (size_t)d * sizeof *y);
         return;
     }
     double t[1024];
-    rotate_bf16_exact(x, t, d, delta, base);
+    rotate_bf16_exact(x, t, d, delta, base, il);
     for (int i = 0; i < d; ++i)
         y[i] = kvo_round_bf16(t[i]);
+}
+
+/* y = rnd(R(δ)·x) on bf16 vectors.  R(0) is the identity, bit for bit
+ * (this also fixes the sign of zeros).  x and y may alias. */
+void kvo_rotate_bf16(const uint16_t *x, uint16_t *y, int d, int64_t delta, double base)
+{
+    rotate_bf16_pairs(x, y, d, delta, base, 0);
+}
+
+/* The same with the interleaved pairing. */
+void kvo_rotate_bf16_il(const uint16_t *x, uint16_t *y, int d, int64_t delta, double base)
+{
+    rotate_bf16_pairs(x, y, d, delta, base, 1);
 }
 
 /* ------------------------------------------------------------------ */
@@ -175,6 +205,7 @@ typedef struct {
     double rope_base;    /* 10000, 500000, ... */
     uint16_t *copy;      /* [L][num_slots][copy_dim] */
     uint16_t *rot;       /* [L][num_slots][rot_heads*rot_d] */
+    int pair_convention; /* 0: rotate-half (x[j], x[j+d/2]); 1: interleaved (x[2j], x[2j+1]) */
 } kvo_pool;
 
 /* Rank-m patch factors (Kamera §2: U_m V_mᵀ), one pair per channel.
@@ -220,7 +251,8 @@ static int pool_ok(const kvo_pool *p)
     return p && p->copy && p->rot && p->num_layers > 0 && p->num_slots > 0 &&
            p->block_size > 0 && p->copy_dim >= 0 && p->rot_heads > 0 &&
            p->rot_d > 0 && p->rot_d % 2 == 0 && p->rot_d <= 1024 &&
-           p->num_slots % p->block_size == 0 && p->rope_base > 0.0;
+           p->num_slots % p->block_size == 0 && p->rope_base > 0.0 &&
+           (p->pair_convention == 0 || p->pair_convention == 1);
 }
 
 /* Physical slot of logical position pos in the block table row bt_row, or -1
@@ -286,7 +318,7 @@ int kvo_relocate(const kvo_pool *src, kvo_pool *dst, int num_chunks, const int32
         return KVO_ERR_INVALID;
     if (src->num_layers != dst->num_layers || src->copy_dim != dst->copy_dim ||
         src->rot_heads != dst->rot_heads || src->rot_d != dst->rot_d ||
-        src->rope_base != dst->rope_base)
+        src->rope_base != dst->rope_base || src->pair_convention != dst->pair_convention)
         return KVO_ERR_INVALID;
     if (tok_off[0] != 0)
         return KVO_ERR_INVALID;
@@ -330,7 +362,8 @@ int kvo_relocate(const kvo_pool *src, kvo_pool *dst, int num_chunks, const int32
                             for (int i = 0; i < rd; ++i)
                                 ex[i] = kvo_bf16_to_f64(sr[h * rd + i]);
                         } else {
-                            rotate_bf16_exact(sr + h * rd, ex, rd, delta[c], src->rope_base);
+                            rotate_bf16_exact(sr + h * rd, ex, rd, delta[c], src->rope_base,
+                                              src->pair_convention);
                         }
                         for (int i = 0; i < rd; ++i)
                             dr[h * rd + i] =
@@ -338,7 +371,8 @@ int kvo_relocate(const kvo_pool *src, kvo_pool *dst, int num_chunks, const int32
                                                                   u_row(patch, tok_off, c, t),
                                                                   v_slot(patch, c), h * rd + i));
                     } else {
-                        kvo_rotate_bf16(sr + h * rd, dr + h * rd, rd, delta[c], src->rope_base);
+                        rotate_bf16_pairs(sr + h * rd, dr + h * rd, rd, delta[c],
+                                          src->rope_base, src->pair_convention);
                     }
                 }
             }
@@ -482,7 +516,8 @@ int kvo_splice(kvo_pool *pool, int num_seqs, const int32_t *block_tables, int ma
                 memcpy(nc + p * cd, copy_row(pool, l, s), (size_t)cd * sizeof *nc);
                 const uint16_t *sr = rot_row(pool, l, s);
                 for (int h = 0; h < rh; ++h)
-                    kvo_rotate_bf16(sr + h * rd, nr + p * rw + h * rd, rd, delta, pool->rope_base);
+                    rotate_bf16_pairs(sr + h * rd, nr + p * rw + h * rd, rd, delta,
+                                      pool->rope_base, pool->pair_convention);
             }
             for (int64_t p = 0; p < new_len; ++p) {
                 int64_t s = slot_of(pool, bt, max_blocks, p);
@@ -618,8 +653,8 @@ int kvo_splice_composed(kvo_pool *pool, int num_seqs, int num_dirs, const int32_
                 }
                 memcpy(nc + p * cd, sc, (size_t)cd * sizeof *nc);
                 for (int h = 0; h < rh; ++h)
-                    kvo_rotate_bf16(sr + h * rd, nrr + p * rw + h * rd, rd, p - cur[p].written,
-                                    pool->rope_base);
+                    rotate_bf16_pairs(sr + h * rd, nrr + p * rw + h * rd, rd, p - cur[p].written,
+                                      pool->rope_base, pool->pair_convention);
             }
             for (int64_t p = 0; p < len; ++p) {
                 const int64_t s = slot_of(pool, bt, max_blocks, p);

@@ -64,29 +64,31 @@ def theta(base: float, j: int, d: int) -> float:
     return base ** (-2.0 * j / d)
 
 
-def rotate_exact(x, delta: int, base: float):
-    """R(δ)·x for a real rotary vector x (list of floats), as complex products."""
+def rotate_exact(x, delta: int, base: float, il: bool = False):
+    """R(δ)·x for a real rotary vector x (list of floats), as complex products:
+    z_j = x[j] + i·x[j+d/2] (rotate-half) or x[2j] + i·x[2j+1] (il)."""
     d = len(x)
     h = d // 2
     out = [0.0] * d
     for j in range(h):
-        z = complex(x[j], x[j + h]) * cmath.exp(1j * (delta * theta(base, j, d)))
-        out[j], out[j + h] = z.real, z.imag
+        re, im = (2 * j, 2 * j + 1) if il else (j, j + h)
+        z = complex(x[re], x[im]) * cmath.exp(1j * (delta * theta(base, j, d)))
+        out[re], out[im] = z.real, z.imag
     return out
 
 
-def rotate_bits(xbits, delta: int, base: float):
+def rotate_bits(xbits, delta: int, base: float, il: bool = False):
     """bf16 rotation on bit patterns; R(0) keeps the bits."""
     if delta == 0:
         return [int(b) for b in xbits]
-    y = rotate_exact([bf16_bits_to_float(b) for b in xbits], delta, base)
+    y = rotate_exact([bf16_bits_to_float(b) for b in xbits], delta, base, il)
     return [round_bf16(v) for v in y]
 
 
-def rotate_row(rowbits, heads: int, d: int, delta: int, base: float):
+def rotate_row(rowbits, heads: int, d: int, delta: int, base: float, il: bool = False):
     out = []
     for h in range(heads):
-        out += rotate_bits(rowbits[h * d:(h + 1) * d], delta, base)
+        out += rotate_bits(rowbits[h * d:(h + 1) * d], delta, base, il)
     return out
 
 
@@ -95,7 +97,7 @@ def slot(bt_row, pos: int, block: int) -> int:
 
 
 def relocate(src_copy, src_rot, dst_copy, dst_rot, block, heads, d, base, tok_off, src_slots,
-             chunk_req, chunk_dst_pos, delta, bt, patch=None):
+             chunk_req, chunk_dst_pos, delta, bt, patch=None, il=False):
     """Gather + rotate (+ patch) into copies of the destination arrays.
 
     ``patch`` = (U[2], V[2]) with U[ch] (L, T, m) and V[ch] (L, C, width, m)
@@ -121,15 +123,15 @@ def relocate(src_copy, src_rot, dst_copy, dst_rot, block, heads, d, base, tok_of
                     ex = []
                     for h in range(heads):
                         seg = [bf16_bits_to_float(b) for b in rb[h * d:(h + 1) * d]]
-                        ex += seg if delta[c] == 0 else rotate_exact(seg, int(delta[c]), base)
+                        ex += seg if delta[c] == 0 else rotate_exact(seg, int(delta[c]), base, il)
                     dr[l, o] = [round_bf16(e + float(a)) for e, a in zip(ex, add)]
                 else:
-                    dr[l, o] = rotate_row(rb, heads, d, int(delta[c]), base)
+                    dr[l, o] = rotate_row(rb, heads, d, int(delta[c]), base, il)
     return dc, dr
 
 
 def splice(copy, rot, block, heads, d, base, bt, seq_lens, s_start, s_end, stub_len, stub_copy,
-           stub_rot):
+           stub_rot, il=False):
     """List-slicing restatement of one AMORTIZE directive per sequence."""
     pc, pr = copy.copy(), rot.copy()
     L = copy.shape[0]
@@ -142,7 +144,7 @@ def splice(copy, rot, block, heads, d, base, bt, seq_lens, s_start, s_end, stub_
             old = [(list(pc[l, slot(bt[q], p, block)]), list(pr[l, slot(bt[q], p, block)]))
                    for p in range(n)]
             stub = [(list(stub_copy[l, off + k]), list(stub_rot[l, off + k])) for k in range(nr)]
-            moved = [(cpy, rotate_row(rt, heads, d, delta, base)) for cpy, rt in old[b:]]
+            moved = [(cpy, rotate_row(rt, heads, d, delta, base, il)) for cpy, rt in old[b:]]
             new = old[:a] + stub + moved
             for p, (cpy, rt) in enumerate(new):
                 s = slot(bt[q], p, block)

@@ -29,7 +29,7 @@ MUTANTS = [
     ("double-rounding", "double a = fabs(v);", "double a = (double)(float)fabs(v);", 0),
     ("no-subnormals", "if (E < -126)\n        E = -126;", "if (E < -150)\n        E = -150;", 0),
     ("identity-lost", "if (delta == 0) {\n        memmove", "if (0) {\n        memmove", 0),
-    ("splice-rotates-by-minus-delta", "rd, delta, pool->rope_base);", "rd, -delta, pool->rope_base);", 0),
+    ("splice-rotates-by-minus-delta", "nr + p * rw + h * rd, rd, delta,", "nr + p * rw + h * rd, rd, -delta,", 0),
     ("splice-reads-span", "slot_of(pool, bt, max_blocks, s_end[q] + k)", "slot_of(pool, bt, max_blocks, s_start[q] + k)", 0),
     ("stub-reversed", "stub_copy + ((int64_t)l * total_stub + stub_base + k) * cd",
      "stub_copy + ((int64_t)l * total_stub + stub_base + (n_r - 1 - k)) * cd", 0),
@@ -45,6 +45,8 @@ MUTANTS = [
      "kvo_round_bf16(kvo_bf16_to_f64(kvo_round_bf16(ex[i])) + patch_term(patch, 1, l,", 0),
     ("relocate-ignores-copy-patch", "if (has_patch(patch, 0)) {\n                    for (int col = 0; col < cd; ++col)\n                        dc[col]",
      "if (0) {\n                    for (int col = 0; col < cd; ++col)\n                        dc[col]", 0),
+    ("interleaved-partner", "double even = x[2 * j], odd = x[2 * j + 1];", "double even = x[2 * j], odd = x[(2 * j + 3) % d];", 0),
+    ("interleaved-sin-sign", "y[2 * j] = even * c - odd * s;", "y[2 * j] = even * c + odd * s;", 0),
     ("composed-origin-position-zero", "cur[p].written = p;", "cur[p].written = 0;", 0),
     ("composed-stub-never-rotated", "rd, p - cur[p].written,", "rd, cur[p].src >= 0 ? p - cur[p].written : 0,", 0),
     ("composed-stub-rows-ignore-sequence", "if (i2 < i || (i2 == i && q2 < q))", "if (i2 < i)", 0),
@@ -74,6 +76,8 @@ def _pins():
         ("splice-forget", P.test_splice_forget_truncates_without_moving_data),
         ("splice-successive", P.test_successive_directives_round_between_calls),
         ("splice-brute", P.test_splice_brute_force_every_directive),
+        ("interleaved-complex", lambda o: P.test_interleaved_rotation_is_complex_multiplication(o, 64)),
+        ("interleaved-ops", P.test_interleaved_relocate_and_splice_match_the_restatement),
         ("composed-single", P.test_composed_single_directive_is_the_splice),
         ("composed-batch", P.test_composed_three_directives_batch_gqa),
         ("composed-brute", P.test_composed_brute_force_two_directives),

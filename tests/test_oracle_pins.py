@@ -729,6 +729,65 @@ def test_composed_checks_final_capacity_and_each_directive(oracle):
     assert np.array_equal(pool.copy, before_c) and np.array_equal(pool.rot, before_r)
 
 
+# ---------------------------------------------------------------------------
+# Interleaved pairing: pair j = (x[2j], x[2j+1]), same θ_j
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("d", [8, 64, 128])
+def test_interleaved_rotation_is_complex_multiplication(oracle, d):
+    rng = np.random.default_rng(160 + d)
+    x = synth.bits(synth.bf16_normal((d,), 161 + d)).copy()
+    for delta in (1, -7, 999, 65536, -100000):
+        got = oracle.rotate_bf16(x, delta, 10000.0, interleaved=True)
+        assert got.tolist() == ind.rotate_bits(x, delta, 10000.0, il=True), delta
+    assert oracle.rotate_bf16(x, 0, 10000.0, interleaved=True).tolist() == x.tolist()
+    del rng
+
+
+def test_interleaved_is_rotate_half_under_the_index_permutation(oracle):
+    # moving x[2j] -> j and x[2j+1] -> j + d/2 turns one pairing into the other
+    d = 64
+    perm = np.concatenate([np.arange(0, d, 2), np.arange(1, d, 2)])
+    for seed in range(4):
+        x = synth.bits(synth.bf16_normal((d,), 170 + seed)).copy()
+        for delta in (3, -4096, 77777):
+            il = oracle.rotate_bf16(x, delta, 500000.0, interleaved=True)
+            half = oracle.rotate_bf16(x[perm], delta, 500000.0)
+            back = np.empty_like(half)
+            back[perm] = half
+            assert np.array_equal(il, back)
+            assert not np.array_equal(il, oracle.rotate_bf16(x, delta, 500000.0))
+
+
+def test_interleaved_relocate_and_splice_match_the_restatement(oracle):
+    heads, d, cd = 2, 8, 8
+    wl, sc, sr, dc, dr = _tiny_relocate_case(181, heads, d, cd)
+    src = O.Pool(sc, sr, 4, heads, d, 10000.0, pair_convention=1)
+    dst = O.Pool(dc.copy(), dr.copy(), 4, heads, d, 10000.0, pair_convention=1)
+    args = (wl.tok_off, wl.src_slots, wl.chunk_req, wl.chunk_dst_pos, wl.delta, wl.block_tables)
+    assert oracle.relocate(src, dst, *args) == O.OK
+    wc, wr = ind.relocate(sc, sr, dc, dr, 4, heads, d, 10000.0, *args, il=True)
+    assert np.array_equal(dst.copy, wc) and np.array_equal(dst.rot, wr)
+    # conventions must agree between the pools
+    mixed = O.Pool(dc.copy(), dr.copy(), 4, heads, d, 10000.0)
+    assert oracle.relocate(src, mixed, *args) == O.ERR_INVALID
+    lens = [13, 21]
+    ss, cp, rt = _splice_pool(182, lens, 9, heads, d, cd)
+    d0 = synth.random_directives(183, np.asarray(lens, np.int32), 0, 10, 0, 7)
+    tot = int(d0.stub_len.sum())
+    stc = synth.bits(synth.bf16_normal((2, max(tot, 1), cd), 184)).copy()[:, :tot]
+    str_ = synth.bits(synth.bf16_normal((2, max(tot, 1), heads * d), 185)).copy()[:, :tot]
+    stc, str_ = np.ascontiguousarray(stc), np.ascontiguousarray(str_)
+    pool = O.Pool(cp.copy(), rt.copy(), 4, heads, d, 10000.0, pair_convention=1)
+    seq = np.array(lens, np.int32)
+    assert oracle.splice(pool, ss.block_tables, seq, d0.s_start, d0.s_end, d0.stub_len, stc,
+                         str_) == O.OK
+    wc, wr, wl2 = ind.splice(cp, rt, 4, heads, d, 10000.0, ss.block_tables, lens, d0.s_start,
+                             d0.s_end, d0.stub_len, stc, str_, il=True)
+    assert seq.tolist() == wl2
+    assert np.array_equal(pool.copy, wc) and np.array_equal(pool.rot, wr)
+
+
 def test_mla_row_split():
     # Irminsul §2.1: cKV is 89% of the MLA row, k_r 11%
     assert round(512 / 576 * 100) == 89 and round(64 / 576 * 100) == 11

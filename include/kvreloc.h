@@ -32,10 +32,12 @@
  *    kernel traps.
  *  - One workspace serves one call at a time: calls that share a workspace
  *    must be ordered (same stream, or synchronised).
- *  - Rotation convention: "rotate-half".  On a rotary vector of d elements,
- *    pair j is (x[j], x[j+d/2]), j < d/2, with frequency θ_j = base^(-2j/d);
- *    R(δ) turns pair j by the angle δ·θ_j:
+ *  - Rotation convention: "rotate-half" by default.  On a rotary vector of d
+ *    elements, pair j is (x[j], x[j+d/2]), j < d/2, with frequency
+ *    θ_j = base^(-2j/d); R(δ) turns pair j by the angle δ·θ_j:
  *       y[j] = x[j]·cos - x[j+d/2]·sin,  y[j+d/2] = x[j]·sin + x[j+d/2]·cos.
+ *    A pool with pair_convention = 1 stores interleaved pairs (x[2j], x[2j+1])
+ *    instead (same θ_j); source and destination pools must agree.
  *    The angle and its cosine/sine are formed in fp64 (one small table per
  *    call); the rotation runs in fp32 registers with compensated products and
  *    one round-to-nearest-even to bf16.  R(0) is the identity, bit for bit.
@@ -99,6 +101,8 @@ typedef struct {
     int32_t rot_heads;         /* 1 (MLA) or H (GQA) */
     int32_t rot_head_dim;      /* 64 (MLA) or 128 (GQA) */
     double rope_base;          /* 10000, 500000, ... */
+    int32_t pair_convention;   /* 0: rotate-half pairs (x[j], x[j+d/2]);
+                                  1: interleaved pairs (x[2j], x[2j+1]), same θ_j */
 } kv_pool_desc;
 
 /* Rank-m patch factors, one (U, V) pair per channel: index 0 patches the

@@ -49,6 +49,7 @@ class kv_pool_desc(C.Structure):
         ("rot_heads", C.c_int32),
         ("rot_head_dim", C.c_int32),
         ("rope_base", C.c_double),
+        ("pair_convention", C.c_int32),
     ]
 
 
@@ -153,17 +154,18 @@ def _check(status: int, where: str) -> None:
 # ---------------------------------------------------------------------------
 
 def pool_desc(copy: torch.Tensor, rot: torch.Tensor, block_size: int, rot_heads: int,
-              rope_base: float) -> kv_pool_desc:
+              rope_base: float, pair_convention: int = 0) -> kv_pool_desc:
     """Describe a pool from two bf16 views: ``copy`` [L][slots][copy_dim] and
     ``rot`` [L][slots][rot_heads*head_dim] (any strides with a unit last stride;
-    e.g. the two column ranges of one fused [L][slots][576] MLA tensor)."""
+    e.g. the two column ranges of one fused [L][slots][576] MLA tensor).
+    ``pair_convention`` 1: rotary pairs stored interleaved (x[2j], x[2j+1])."""
     assert copy.dtype == torch.bfloat16 and rot.dtype == torch.bfloat16
     assert copy.dim() == 3 and rot.dim() == 3 and copy.stride(2) == 1 and rot.stride(2) == 1
     assert copy.shape[:2] == rot.shape[:2]
     L, S, cd = copy.shape
     d = kv_pool_desc(L, block_size, S, copy.data_ptr(), copy.stride(0), copy.stride(1), cd,
                      rot.data_ptr(), rot.stride(0), rot.stride(1), rot_heads,
-                     rot.shape[2] // rot_heads, float(rope_base))
+                     rot.shape[2] // rot_heads, float(rope_base), int(pair_convention))
     d._tensors = (copy, rot)  # the descriptor keeps the memory it points at alive
     return d
 

@@ -43,7 +43,7 @@ bool pool_ok(const kv_pool_desc *p)
     if (p->copy_dim <= 0 || p->copy_dim % 8 != 0 || p->rot_heads <= 0 || p->rot_head_dim <= 0 ||
         p->rot_head_dim % 16 != 0)
         return false;
-    if (!(p->rope_base > 0.0))
+    if (!(p->rope_base > 0.0) || (p->pair_convention != 0 && p->pair_convention != 1))
         return false;
     if (!p->copy_base || !p->rot_base || !aligned16(p->copy_base) || !aligned16(p->rot_base))
         return false;
@@ -89,6 +89,7 @@ PoolView view_of(const kv_pool_desc *p)
     v.num_blocks = p->num_slots / p->block_size;
     v.block = p->block_size;
     v.num_layers = p->num_layers;
+    v.il = p->pair_convention;
     return v;
 }
 
@@ -157,7 +158,7 @@ kv_status relocate_impl(const kv_pool_desc *src, const kv_pool_desc *dst, int32_
         return KV_ERR_INVALID_ARG;
     if (src->num_layers != dst->num_layers || src->copy_dim != dst->copy_dim ||
         src->rot_heads != dst->rot_heads || src->rot_head_dim != dst->rot_head_dim ||
-        src->rope_base != dst->rope_base)
+        src->rope_base != dst->rope_base || src->pair_convention != dst->pair_convention)
         return KV_ERR_INVALID_ARG;
     RowKind kind;
     if (!row_kind(src, &kind))

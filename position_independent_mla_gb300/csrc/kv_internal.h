@@ -29,6 +29,7 @@ struct PoolView {
     int64_t num_blocks;
     int32_t block;
     int32_t num_layers;
+    int32_t il; // rotary pairs interleaved (x[2j], x[2j+1]) instead of rotate-half
 };
 
 struct PatchView {

@@ -539,7 +539,10 @@ static cudaError_t launch_geo(const RelocParams &p, TcLaunch tl, cudaStream_t st
 bool patch_tc_supported(const RelocParams &p, RowKind kind)
 {
     (void)kind;
-    return p.patched && p.patch.m <= tc::KP && p.src.num_layers <= 65535;
+    // the epilogue turns rotate-half pairs; relocations of interleaved rows
+    // take the token-tiled kernel (an in-place patch rotates nothing)
+    return p.patched && p.patch.m <= tc::KP && p.src.num_layers <= 65535 &&
+           (p.in_place || !p.dst.il);
 }
 
 int patch_tc_launches(RowKind kind) { return kind == RowKind::Mla ? 2 : 1; }

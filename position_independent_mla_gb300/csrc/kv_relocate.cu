@@ -50,7 +50,7 @@ cudaError_t launch_delta_table(const TableParams &p, cudaStream_t stream)
 // Relocation / in-place patch
 // ---------------------------------------------------------------------------
 
-template <class G, bool PATCH>
+template <class G, bool PATCH, bool IL>
 __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const __grid_constant__ RelocParams p)
 {
     __shared__ int64_t s_src[G::T];
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const
         TileRegs<G> regs;
         load_tile<G>(from, s_src, regs);
         pa.layer = l;
-        store_tile<G, PATCH>(to, s_dst, regs, &s_cs[0][0], G::kCsRow, s_ident, pa);
+        store_tile<G, PATCH, true, IL>(to, s_dst, regs, &s_cs[0][0], G::kCsRow, s_ident, pa);
     }
 }
 
@@ -146,11 +146,14 @@ static cudaError_t launch_reloc_shape(const RelocParams &p, cudaStream_t stream)
         return cudaSuccess;
     if (tiles > 0x7FFFFFFFll)
         return cudaErrorInvalidConfiguration;
-    if (p.patched)
-        relocate_kernel<G, true><<<(unsigned)tiles, kThreads, 0, stream>>>(p);
-    else
-        relocate_kernel<G, false><<<(unsigned)tiles, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return with_bool(p.dst.il != 0, [&](auto il) {
+        constexpr bool IL = decltype(il)::value;
+        if (p.patched)
+            relocate_kernel<G, true, IL><<<(unsigned)tiles, kThreads, 0, stream>>>(p);
+        else
+            relocate_kernel<G, false, IL><<<(unsigned)tiles, kThreads, 0, stream>>>(p);
+        return cudaGetLastError();
+    });
 }
 
 cudaError_t launch_relocate(const RelocParams &p, RowKind kind, cudaStream_t stream)

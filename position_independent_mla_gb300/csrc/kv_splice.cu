@@ -33,7 +33,7 @@ namespace kvr {
 
 constexpr uint32_t kWarps = kThreads / 32;
 
-template <class G>
+template <class G, bool IL>
 __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const __grid_constant__ SpliceParams p)
 {
     __shared__ uint32_t s_ticket;
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
         }
         __syncthreads();
         if (!s_abort)
-            store_tile<G, false>(pool_l, s_dst, regs, s_cs, 0, s_ident, none);
+            store_tile<G, false, true, IL>(pool_l, s_dst, regs, s_cs, 0, s_ident, none);
     }
 }
 
@@ -184,8 +184,11 @@ cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stre
         return cudaErrorInvalidConfiguration;
     const unsigned blocks = (unsigned)p.total_tickets;
     return with_geo(kind, [&](auto g) {
-        splice_kernel<typename decltype(g)::type><<<blocks, kThreads, 0, stream>>>(p);
-        return cudaGetLastError();
+        return with_bool(p.pool.il != 0, [&](auto il) {
+            splice_kernel<typename decltype(g)::type, decltype(il)::value>
+                <<<blocks, kThreads, 0, stream>>>(p);
+            return cudaGetLastError();
+        });
     });
 }
 
@@ -203,7 +206,7 @@ cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stre
 // once, its rotary part turned by its total shift.
 // ---------------------------------------------------------------------------
 
-template <class G>
+template <class G, bool IL>
 __global__ void __launch_bounds__(kThreads, G::kMinBlocks)
 splice_composed_kernel(const __grid_constant__ ComposedParams p)
 {
@@ -293,7 +296,7 @@ splice_composed_kernel(const __grid_constant__ ComposedParams p)
         }
         __syncthreads();
         if (!s_abort)
-            store_tile<G, false>(pool_l, s_dst, regs, s_cs, 0, s_ident, none);
+            store_tile<G, false, true, IL>(pool_l, s_dst, regs, s_cs, 0, s_ident, none);
     }
 }
 
@@ -305,8 +308,11 @@ cudaError_t launch_splice_composed(const ComposedParams &p, RowKind kind, cudaSt
         return cudaErrorInvalidConfiguration;
     const unsigned blocks = (unsigned)p.num_tiles;
     return with_geo(kind, [&](auto g) {
-        splice_composed_kernel<typename decltype(g)::type><<<blocks, kThreads, 0, stream>>>(p);
-        return cudaGetLastError();
+        return with_bool(p.pool.il != 0, [&](auto il) {
+            splice_composed_kernel<typename decltype(g)::type, decltype(il)::value>
+                <<<blocks, kThreads, 0, stream>>>(p);
+            return cudaGetLastError();
+        });
     });
 }
 
@@ -343,7 +349,7 @@ __device__ __forceinline__ int32_t remapped_entry(const int32_t *old, int32_t j,
     return spare(Nb + (j - A - Nb - Db));
 }
 
-template <class G>
+template <class G, bool IL>
 __global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(const __grid_constant__ RemapParams p)
 {
     __shared__ int64_t s_idx[G::T]; // slot of each row (in place, or the stub's target)
@@ -408,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(con
 #pragma unroll
             for (int b = 0; b < LB; ++b)
                 if (l0 + b < Lc)
-                    store_tile<G, false, false>(layer_rows(l0 + b), s_idx, regs[b], s_cs, 0,
+                    store_tile<G, false, false, IL>(layer_rows(l0 + b), s_idx, regs[b], s_cs, 0,
                                                 s_ident, none);
         }
         return;
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(con
                                 rot_row_bytes};
             // the tile's rows are stub rows 0..T-1 counted from stub_l
             load_tile<G>(stub_l, s_src, regs);
-            store_tile<G, false>(pool_l, s_idx, regs, s_cs, 0, s_ident, none);
+            store_tile<G, false, true, IL>(pool_l, s_idx, regs, s_cs, 0, s_ident, none);
         }
     }
 }
@@ -456,9 +462,11 @@ cudaError_t launch_remap(const RemapParams &p, RowKind kind, cudaStream_t stream
         if (p.total_tiles > 0x7FFFFFFFll)
             return cudaErrorInvalidConfiguration;
         cudaError_t e = with_geo(kind, [&](auto g) {
-            remap_data_kernel<typename decltype(g)::type>
-                <<<(unsigned)p.total_tiles, kThreads, 0, stream>>>(p);
-            return cudaGetLastError();
+            return with_bool(p.pool.il != 0, [&](auto il) {
+                remap_data_kernel<typename decltype(g)::type, decltype(il)::value>
+                    <<<(unsigned)p.total_tiles, kThreads, 0, stream>>>(p);
+                return cudaGetLastError();
+            });
         });
         if (e != cudaSuccess)
             return e;

@@ -51,6 +51,18 @@ struct GeoTag {
     using type = G;
 };
 
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
+// Call f(BoolTag<b>{}) with b as a compile-time constant.
+template <class F>
+cudaError_t with_bool(bool b, F &&f)
+{
+    return b ? f(BoolTag<true>{}) : f(BoolTag<false>{});
+}
+
 // Call f(GeoTag<G>{}) with the tile geometry of `kind`.
 template <class F>
 cudaError_t with_geo(RowKind kind, F &&f)
@@ -163,11 +175,32 @@ __device__ __forceinline__ void patch_terms(const PatchView &pv, int ch, int l, 
     }
 }
 
+// Interleaved pairing: the 16-byte vector v of a head holds pairs
+// (x[8v+2i], x[8v+2i+1]) of frequencies 4v+i, i < 4, one pair per 32-bit
+// word, so no partner lane is needed.  cs_row is the row's transposed
+// cos/sin table (entry of frequency f at Geo::cs_index(f)).
+template <class G>
+__device__ __forceinline__ uint4 rotate_vec_il(uint4 x, const float4 *cs_row, int v,
+                                               const float *add)
+{
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 q = cs_row[G::cs_index(4 * v + i)];
+        const uint32_t even = w[i] & 0xFFFFu, odd = w[i] >> 16;
+        out[i] = rotate_one(even, odd, q, true, add[2 * i]) |
+                 (rotate_one(even, odd, q, false, add[2 * i + 1]) << 16);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 // Write a loaded tile: verbatim vectors as they are (plus the patch),
 // rotary vectors turned by the row's cos/sin (a transposed table row at
 // cs + row*cs_row_stride, see Geo::cs_index) unless the row is marked
 // identity.
-template <class G, bool PATCH, bool COPY = true>
+// IL: the rotary pairs are interleaved (x[2j], x[2j+1]) instead of rotate-half.
+template <class G, bool PATCH, bool COPY = true, bool IL = false>
 __device__ __forceinline__ void store_tile(const RowsAt &at, const int64_t *idx,
                                            const TileRegs<G> &regs, const float4 *cs,
                                            int cs_row_stride, const int32_t *ident,
@@ -215,6 +248,8 @@ __device__ __forceinline__ void store_tile(const RowsAt &at, const int64_t *idx,
                 uint4 out;
                 if (ident[row])
                     out = patched ? add_vec(regs.r[k], add) : regs.r[k];
+                else if (IL)
+                    out = rotate_vec_il<G>(regs.r[k], cs + row * cs_row_stride, v, add);
                 else
                     out = rotate_vec(regs.r[k], partner, first,
                                      cs + row * cs_row_stride + fb / 8, G::HV, add);

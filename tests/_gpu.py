@@ -28,7 +28,8 @@ class DevPool:
     """A paged pool on the GPU (MLA: one fused [L][slots][576] tensor; GQA:
     separate V and K tensors) plus its oracle mirror."""
 
-    def __init__(self, shape: str, L: int, slots: int, seed: int, block: int = 64):
+    def __init__(self, shape: str, L: int, slots: int, seed: int, block: int = 64,
+                 pair_convention: int = 0):
         cd, H, d, base = SHAPES[shape]
         self.shape, self.cd, self.H, self.d, self.base, self.block = shape, cd, H, d, base, block
         copy = synth.bf16_normal((L, slots, cd), seed)
@@ -40,8 +41,9 @@ class DevPool:
         else:
             self.copy_view = copy.cuda()
             self.rot_view = rot.cuda()
-        self.desc = kv.pool_desc(self.copy_view, self.rot_view, block, H, base)
-        self.orc = O.Pool(synth.bits(copy).copy(), synth.bits(rot).copy(), block, H, d, base)
+        self.desc = kv.pool_desc(self.copy_view, self.rot_view, block, H, base, pair_convention)
+        self.orc = O.Pool(synth.bits(copy).copy(), synth.bits(rot).copy(), block, H, d, base,
+                          pair_convention)
 
     def gpu_bits(self):
         torch.cuda.synchronize()

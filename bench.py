@@ -67,6 +67,9 @@ KERNEL_SOURCES = {
     "splice_mla_128k": ("kv_splice.cu",) + _COMMON_SOURCES,
     "relocate_gqa_patch": ("kv_patch_tc.cu",) + _COMMON_SOURCES,
     "relocate_mla_patch": ("kv_patch_tc.cu",) + _COMMON_SOURCES,
+    "splice_mla_128k_composed": ("kv_splice.cu",) + _COMMON_SOURCES,
+    "splice_mla_128k_remap": ("kv_splice.cu",) + _COMMON_SOURCES,
+    "window_gqa": ("kv_splice.cu", "kv_patch_tc.cu") + _COMMON_SOURCES,
 }
 
 
@@ -774,8 +777,9 @@ def run_splice_mla_128k_remap(args, rank, world, local):
                    "l2": "inputs larger than L2 (%.1f GB moved per step); cache and block "
                          "tables restored before each step, untimed" % (nbytes / 1e9)},
         "roofline": {"bound": "hbm", "achieved": nbytes / (kms * 1e-3) / 1e9 if kms > 0 else None,
-                     "peak": peak, "unit": "GB/s", "peak_kind": peak_kind, "traffic": None,
-                     "kernel": "remap_data_kernel<MLA> (last round of a step)",
+                     "peak": peak, "unit": "GB/s", "peak_kind": peak_kind,
+                     "traffic": recorded_traffic("splice_mla_128k_remap"),
+                     "kernel": "remap_data_kernel<MLA> (whole step: 4 rounds)",
                      "kernel_ms_last_round": kms, "algorithmic_bytes_per_step": nbytes,
                      "frac": None},
         "e2e": None, "clocks": clk, "gpu_launches": launches,
@@ -859,7 +863,8 @@ def run_splice_mla_128k_composed(args, rank, world, local):
                    "l2": "inputs larger than L2 (%.1f GB moved per step); cache restored "
                          "from a pristine copy before each call, untimed" % (nbytes / 1e9)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": recorded_traffic("splice_mla_128k_composed"),
                      "kernel": "splice_composed_kernel<MLA>", "kernel_ms": kms,
                      "algorithmic_bytes_per_step": nbytes},
         "e2e": {"value": rows * world * K / e2e_s, "unit": "tokens/s",
@@ -1422,7 +1427,7 @@ def run_window_gqa(args, rank, world, local):
                    "l2": "inputs larger than L2 (%.1f GB moved per step)" % (nbytes / 1e9)},
         "roofline": {"bound": "hbm", "achieved": nbytes / (ms * 1e-3) / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": nbytes / (ms * 1e-3) / 1e9 / peak,
-                     "peak_kind": peak_kind, "traffic": None,
+                     "peak_kind": peak_kind, "traffic": recorded_traffic("window_gqa"),
                      "kernel": "remap_data_kernel<GQA> + patch_tc_kernel (whole step)",
                      "algorithmic_bytes_per_step": nbytes},
         "e2e": None, "clocks": clk, "gpu_launches": launches,

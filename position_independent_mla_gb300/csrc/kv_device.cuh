@@ -164,11 +164,10 @@ static __device__ __noinline__ uint32_t rotate_one_exact(uint32_t xb, uint32_t y
 }
 
 // Same result, cheaply: with exact leading products, t + (u + add) is the
-// rotated value to within a few fp32 ulps, so round-to-nearest-even of it is
-// already the correctly rounded bf16 unless it lies within 4 fp32 ulps of a
-// bf16 rounding boundary, is not finite, or comes out of heavy cancellation
-// (|result| below 2^-12 (|x|+|y|)).  Those rare cases (about 1e-4 of values)
-// take the exact path.
+// rotated value to within 2^-23 (|x| + |y| + |add|), so its round-to-nearest-
+// even is already the correctly rounded bf16 unless a bf16 rounding boundary
+// lies within that distance (the interval test below), or it is not finite.
+// Those rare cases (about 2e-4 of values) take the exact path.
 __device__ __forceinline__ uint32_t rotate_one(uint32_t xb, uint32_t yb, float4 cs, bool first,
                                                float add)
 {
@@ -182,13 +181,15 @@ __device__ __forceinline__ uint32_t rotate_one(uint32_t xb, uint32_t yb, float4 
         u = fmaf(x, cs.w, y * cs.y);
     }
     const float s = t + (u + add);
-    const uint32_t b = __float_as_uint(s);
-    const bool near_tie = ((b & 0xFFFFu) - 0x7FFCu) <= 8u;
-    const bool special = (b & 0x7F800000u) == 0x7F800000u;
-    const bool cancels = fabsf(s) < 2.44140625e-4f * (fabsf(x) + fabsf(y)); // 2^-12
-    if (near_tie || special || cancels)
+    // s is within 2^-23 (|x| + |y| + |add|) of the exact value; round both ends
+    // of an interval twice as wide: if they agree, the exact value rounds to
+    // the same bf16 (rounding is monotone).  This also covers cancellation.
+    const float r = 4.76837158203125e-7f * (fabsf(x) + fabsf(y) + fabsf(add)); // 2^-21
+    uint32_t ends;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(ends) : "f"(s + r), "f"(s - r));
+    if (((ends ^ (ends >> 16)) & 0xFFFFu) != 0u || !(fabsf(s) <= 3.40282347e38f))
         return rotate_one_exact(xb, yb, cs, first, add);
-    return (b + 0x7FFFu + ((b >> 16) & 1u)) >> 16;
+    return ends & 0xFFFFu;
 }
 
 // Patched values are held to 1 bf16 ulp (the fp32 patch sum carries its

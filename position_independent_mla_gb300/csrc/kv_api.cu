@@ -221,7 +221,7 @@ kv_status relocate_impl(const kv_pool_desc *src, const kv_pool_desc *dst, int32_
     KV_CUDA(mark(t_ev_start, stream));
     if (patch_tc_supported(rp, kind)) {
         KV_CUDA(launch_patch_tc(rp, kind, stream));
-        t_launches += patch_tc_launches(kind);
+        t_launches += patch_tc_launches(rp, kind);
     } else {
         KV_CUDA(launch_relocate(rp, kind, stream));
         ++t_launches;

@@ -19,7 +19,7 @@ cudaError_t launch_relocate(const RelocParams &p, RowKind kind, cudaStream_t str
 // (larger ranks take launch_relocate's per-element patch).
 bool patch_tc_supported(const RelocParams &p, RowKind kind);
 cudaError_t launch_patch_tc(const RelocParams &p, RowKind kind, cudaStream_t stream);
-int patch_tc_launches(RowKind kind); // kernels one launch_patch_tc issues
+int patch_tc_launches(const RelocParams &p, RowKind kind); // kernels launch_patch_tc issues
 // Launches one ticketed block per tile; `blocks` = p.total_tickets.
 cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stream);
 // Composed splice: one ticketed block per tile of p.tiles.

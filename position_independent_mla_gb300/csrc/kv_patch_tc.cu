@@ -35,19 +35,25 @@ constexpr int KP = 16;                // padded rank (MMA K for 16-bit inputs)
 constexpr int A_BYTES = M * KP * 2;   // one of hi / lo
 constexpr int64_t MMA_WAIT_NS = 1000000000ll;
 
-// NB: columns per block (MMA N, TMEM columns); W: columns per thread;
-// D: rotary head dim of the rotated channel (D == W).
-template <int NB_, int W_>
+// NB: columns per block (MMA N); W: columns per thread; D: rotary head dim of
+// the rotated channel (D == W).  TILES row tiles of M rows are processed per
+// step (each its own A operand and accumulator); a block's 128-thread parts
+// split the columns (GROUPS = NB / W) or the row tiles, not both.
+template <int NB_, int W_, int TILES_ = 1>
 struct TcGeo {
-    static constexpr int NB = NB_, W = W_;
+    static constexpr int NB = NB_, W = W_, TILES = TILES_;
     static constexpr int GROUPS = NB / W;          // column groups per block
-    static constexpr int NT = M * GROUPS;          // threads per block
+    static constexpr int ROWS = M * TILES;         // rows per step
+    static constexpr int NT = M * GROUPS * TILES;  // threads per block
     static constexpr int B_BYTES = NB * KP * 2;    // one of hi / lo
     static constexpr int VECS = W * 2 / 16;        // 16-byte pieces of my columns
     static constexpr int HALF = W / 2;             // frequencies of my head
-    static constexpr int MIN_BLOCKS = 512 / NB < 4 ? 512 / NB : 4; // TMEM: 512 columns / SM
+    static constexpr int TMEM_COLS = NB * TILES;   // accumulator columns
+    static constexpr int MIN_BLOCKS = NT >= 256 ? 2 : (512 / NB < 4 ? 512 / NB : 4);
     static_assert(NB == 64 || NB == 128 || NB == 256, "MMA N");
     static_assert(W % 16 == 0 && NB % W == 0 && (GROUPS == 1 || GROUPS == 2), "groups");
+    static_assert(GROUPS == 1 || TILES == 1, "split columns or rows, not both");
+    static_assert(TMEM_COLS >= 32 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation");
 };
 
 // Byte offset of element (r, k) in a K-major operand made of core matrices
@@ -190,18 +196,18 @@ struct TcLaunch {
     int32_t ch0, nch, slices;
 };
 
-// Dynamic shared memory of one block: A (hi, lo), B (hi, lo), then the row
-// tile, M rows of PITCH bytes.  The 16 spare bytes per row shift consecutive
+// Dynamic shared memory of one block: A (hi, lo) per row tile, B (hi, lo),
+// then the rows of a step, ROWS rows of PITCH bytes.  The 16 spare bytes per row shift consecutive
 // rows by four banks, so a warp reading the same piece of 32 rows is free of
 // bank conflicts.
 template <class G>
 struct TcSmem {
     static constexpr int ROW_BYTES = G::NB * 2;
     static constexpr int PITCH = ROW_BYTES + 16;
-    static constexpr int A_OFF = 0;
-    static constexpr int B_OFF = 2 * A_BYTES;
+    static constexpr int A_OFF = 0;                        // per row tile: hi, lo
+    static constexpr int B_OFF = G::TILES * 2 * A_BYTES;
     static constexpr int X_OFF = B_OFF + 2 * G::B_BYTES;
-    static constexpr int BYTES = X_OFF + M * PITCH;
+    static constexpr int BYTES = X_OFF + G::ROWS * PITCH;
 };
 
 // A block owns NB columns of one channel of one (chunk, layer).  Per tile of
@@ -210,12 +216,11 @@ struct TcSmem {
 // thread rewrites its (row, column group) of the tile in shared memory and
 // threads 0..127 write the rows back with bulk copies.
 template <class G, bool RELOC>
-__global__ void __launch_bounds__(G::NT, G::MIN_BLOCKS)
-patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
+__device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaunch &tl,
+                                              const int bx)
 {
     using S = TcSmem<G>;
     extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char *a_hi = smem + S::A_OFF, *a_lo = a_hi + A_BYTES;
     unsigned char *b_hi = smem + S::B_OFF, *b_lo = b_hi + G::B_BYTES;
     unsigned char *xs = smem + S::X_OFF;
     // cos/sin per pair of frequencies k = (2k, 2k+1): cs_c[k] = (c1, c1', c2, c2'),
@@ -227,10 +232,10 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int per_chunk = tl.nch * tl.slices;
-    const int c = blockIdx.x / per_chunk, l = blockIdx.y;
-    const int ch = tl.ch0 + (blockIdx.x / tl.slices) % tl.nch;
-    const int col0 = (blockIdx.x % tl.slices) * G::NB;
-    if (blockIdx.x == 0 && l == 0 && tid == 0) {
+    const int c = bx / per_chunk, l = blockIdx.y;
+    const int ch = tl.ch0 + (bx / tl.slices) % tl.nch;
+    const int col0 = (bx % tl.slices) * G::NB;
+    if (bx == 0 && l == 0 && tid == 0) {
         if (p.tok_off[0] != 0 || p.tok_off[p.num_chunks] != p.total_tokens)
             set_status(p.status, kStatusOutOfRange);
     }
@@ -247,9 +252,12 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
     const int64_t pos0 = p.chunk_dst_pos[c];
     const bool rotate = RELOC && ch == 1 && p.delta[c] != 0;
     const int m = p.patch.m;
-    const bool owner = tid < M;             // gathers / writes back row `tid`
-    const int row = (warp & 3) * 32 + lane; // my row in the rewrite = TMEM lane
-    const int grp = warp >> 2;              // my column group
+    const bool owner = tid < G::ROWS;           // gathers / writes back row `tid`
+    const int lane_row = (warp & 3) * 32 + lane; // my TMEM lane
+    const int part = warp >> 2;                  // my 128-thread part of the block
+    const int rt = G::TILES > 1 ? part : 0;      // my row tile
+    const int grp = G::TILES > 1 ? 0 : part;     // my column group
+    const int row = rt * M + lane_row;           // my row in the rewrite
     const int cg = grp * G::W;
     const PoolView &sp = RELOC ? p.src : p.dst;
     const char *src_base = (ch == 0 ? sp.copy + (int64_t)l * sp.copy_ls
@@ -282,7 +290,8 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
     const uint32_t bar_x = (uint32_t)__cvta_generic_to_shared(&s_bar[0]);
     const uint32_t bar_mma = (uint32_t)__cvta_generic_to_shared(&s_bar[1]);
     if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar_x), "r"(M) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar_x), "r"(G::ROWS)
+                     : "memory");
         asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_mma) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_ok = 1;
@@ -290,7 +299,7 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
     if (patched && warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          (uint32_t)__cvta_generic_to_shared(&s_tmem)),
-                     "r"((uint32_t)G::NB)
+                     "r"((uint32_t)G::TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -298,12 +307,13 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
     __syncthreads();
     fence_after();
     const uint32_t tmem = patched ? s_tmem : 0u;
-    const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)cg;
+    const uint32_t t_row =
+        tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(rt * G::NB + cg);
 
     // slots of row `tid` of tile t (owners only); a bad index is reported and
     // its row skipped
     auto row_slots = [&](int64_t t, int64_t &src, int64_t &dst) {
-        const int64_t i = t * M + tid;
+        const int64_t i = t * G::ROWS + tid;
         src = dst = -1;
         if (i >= n)
             return;
@@ -321,7 +331,7 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
         }
     };
 
-    const int64_t ntiles = (n + M - 1) / M;
+    const int64_t ntiles = (n + G::ROWS - 1) / G::ROWS;
     unsigned char *my_row = xs + tid * S::PITCH;                   // owner's row
     unsigned char *xr = xs + row * S::PITCH + cg * 2;              // my part in the rewrite
     uint4 *xq = reinterpret_cast<uint4 *>(xr);
@@ -346,9 +356,11 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
         }
         if (patched) {
             // A operand: the tile's U rows split into bf16 hi / lo (zero past the chunk)
-            for (int e = tid; e < M * 2; e += G::NT) {
+            for (int e = tid; e < G::ROWS * 2; e += G::NT) {
                 const int r = e >> 1, k0 = (e & 1) * 8;
-                const int64_t i = t * M + r;
+                const int64_t i = t * G::ROWS + r;
+                unsigned char *a_hi = smem + S::A_OFF + (r / M) * 2 * A_BYTES;
+                unsigned char *a_lo = a_hi + A_BYTES;
                 float u[8];
                 if (i < n) {
                     load_factor8(p.patch.u[ch] + (int64_t)l * p.patch.u_ls[ch] +
@@ -359,16 +371,22 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
                     for (int q = 0; q < 8; ++q)
                         u[q] = 0.0f;
                 }
-                split_store8(u, a_hi + kmajor_off(r, k0), a_lo + kmajor_off(r, k0));
+                split_store8(u, a_hi + kmajor_off(r % M, k0), a_lo + kmajor_off(r % M, k0));
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             fence_before();
             __syncthreads(); // A complete; the previous tile's accumulator reads are done
             if (tid == 0) {
                 fence_after();
-                mma_bf16<G::NB>(tmem, smem_desc(a_hi), smem_desc(b_hi), 0u);
-                mma_bf16<G::NB>(tmem, smem_desc(a_hi), smem_desc(b_lo), 1u);
-                mma_bf16<G::NB>(tmem, smem_desc(a_lo), smem_desc(b_hi), 1u);
+#pragma unroll
+                for (int q = 0; q < G::TILES; ++q) {
+                    const unsigned char *a_hi = smem + S::A_OFF + q * 2 * A_BYTES;
+                    const unsigned char *a_lo = a_hi + A_BYTES;
+                    const uint32_t d = tmem + (uint32_t)(q * G::NB);
+                    mma_bf16<G::NB>(d, smem_desc(a_hi), smem_desc(b_hi), 0u);
+                    mma_bf16<G::NB>(d, smem_desc(a_hi), smem_desc(b_lo), 1u);
+                    mma_bf16<G::NB>(d, smem_desc(a_lo), smem_desc(b_hi), 1u);
+                }
                 asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar_mma)
                              : "memory");
                 if (!mbar_wait(bar_mma, ph_mma, MMA_WAIT_NS)) {
@@ -505,8 +523,54 @@ patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
     __syncthreads();
     if (patched && warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"((uint32_t)G::NB)
+                     "r"((uint32_t)G::TMEM_COLS)
                      : "memory");
+}
+
+template <class G, bool RELOC>
+__global__ void __launch_bounds__(G::NT, G::MIN_BLOCKS)
+patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
+{
+    patch_tc_body<G, RELOC>(p, tl, (int)blockIdx.x);
+}
+
+// MLA rows in one launch: the first n_kv blocks take the latent c_KV in
+// slices of 256 columns (GA), the others the 64-column k_pe in two row tiles
+// per step (GB), so the small k_pe blocks run alongside the c_KV traffic.
+using GeoMlaKv = TcGeo<256, 128>;
+using GeoMlaPe = TcGeo<64, 64, 2>;
+static_assert(GeoMlaKv::NT == GeoMlaPe::NT, "one block shape");
+
+// Blocks 3c, 3c+1: chunk c's two c_KV slices; block 3c+2: its k_pe.
+template <bool RELOC>
+__global__ void __launch_bounds__(GeoMlaKv::NT, 2)
+patch_tc_mla_kernel(const __grid_constant__ RelocParams p)
+{
+    const int c = (int)blockIdx.x / 3, j = (int)blockIdx.x % 3;
+    if (j < 2)
+        patch_tc_body<GeoMlaKv, RELOC>(p, TcLaunch{0, 1, 2}, 2 * c + j);
+    else
+        patch_tc_body<GeoMlaPe, RELOC>(p, TcLaunch{1, 1, 1}, c);
+}
+
+static cudaError_t launch_mla(const RelocParams &p, cudaStream_t stream)
+{
+    const int64_t blocks = (int64_t)p.num_chunks * 3;
+    if (blocks > 0x7FFFFFFFll)
+        return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)blocks, (unsigned)p.src.num_layers);
+    constexpr int smem = TcSmem<GeoMlaKv>::BYTES > TcSmem<GeoMlaPe>::BYTES
+                             ? TcSmem<GeoMlaKv>::BYTES
+                             : TcSmem<GeoMlaPe>::BYTES;
+    return with_bool(p.in_place == 0, [&](auto reloc) {
+        constexpr bool R = decltype(reloc)::value;
+        cudaError_t e = cudaFuncSetAttribute(patch_tc_mla_kernel<R>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        patch_tc_mla_kernel<R><<<grid, GeoMlaKv::NT, smem, stream>>>(p);
+        return cudaGetLastError();
+    });
 }
 
 template <class G>
@@ -545,7 +609,10 @@ bool patch_tc_supported(const RelocParams &p, RowKind kind)
            (p.in_place || !p.dst.il);
 }
 
-int patch_tc_launches(RowKind kind) { return kind == RowKind::Mla ? 2 : 1; }
+int patch_tc_launches(const RelocParams &p, RowKind kind)
+{
+    return (kind == RowKind::Mla && p.in_place) ? 2 : 1;
+}
 
 cudaError_t launch_patch_tc(const RelocParams &p, RowKind kind, cudaStream_t stream)
 {
@@ -556,7 +623,12 @@ cudaError_t launch_patch_tc(const RelocParams &p, RowKind kind, cudaStream_t str
         const int32_t slices = kind == RowKind::Gqa ? 4 : kind == RowKind::Gqa4 ? 2 : 16;
         return tc::launch_geo<tc::TcGeo<256, 128>>(p, tc::TcLaunch{0, 2, slices}, stream);
     }
-    // MLA: the 512-wide latent as 2 slices of 256, the 64-wide k_pe as one slice
+    // MLA relocation: the 512-wide latent as 2 slices of 256 and the 64-wide
+    // k_pe in one launch, so the k_pe blocks run alongside the c_KV traffic.
+    // In place (no gather, no rotation) the k_pe rows are light enough that a
+    // launch of their own, four blocks per SM, is faster.
+    if (!p.in_place)
+        return tc::launch_mla(p, stream);
     cudaError_t e = tc::launch_geo<tc::TcGeo<256, 128>>(p, tc::TcLaunch{0, 1, 2}, stream);
     if (e != cudaSuccess)
         return e;

@@ -148,7 +148,7 @@ def test_standalone_patch(orc, shape):
                 dev["chunk_dst_pos"], dev["block_tables"], wl.block_tables.shape[0],
                 wl.block_tables.shape[1], pd, ws)
     assert kv.kv_get_device_status(ws) == kv.KV_OK
-    # one kernel per distinct channel width: MLA rows are 512 + 64 wide, GQA 1024 + 1024
+    # in place, MLA's c_KV and k_pe slices are launched separately
     assert kv.kv_last_launch_count() == (2 if shape == "mla" else 1)
     assert orc.patch_apply(dst.orc, wl.tok_off, wl.chunk_req, wl.chunk_dst_pos, wl.block_tables,
                            O.Patch(m, [x.numpy() for x in us],

@@ -52,3 +52,16 @@ def test_shards_cover_units_once(n_units):
     assert sorted(flat) == list(range(n_units))
     assert abs(len(got[0]) - len(got[1])) <= 1
     assert t == 2.0
+
+
+def test_oracle_on_every_core_counts_every_unit():
+    """The CPU baseline's process pool: each of its processes relocates its own
+    independent sample behind one barrier, and the round reports every token."""
+    import bench
+
+    cores = bench.OracleCores(2)
+    try:
+        ntok, dt = cores.run(16, 3)
+    finally:
+        cores.close()
+    assert ntok == 32 and dt > 0

@@ -260,6 +260,76 @@ __device__ __forceinline__ uint4 rotate_vec(uint4 mine, uint4 other, bool first,
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// Pair-packed cos/sin (rows without a patch term).  For word k of a vector
+// (its elements e0 = 2k and e1 = 2k + 1) the shared-memory row holds
+//   cs[(2k)   * step] = (c1[e0], c1[e1], s1[e0], s1[e1])
+//   cs[(2k+1) * step] = (c2[e0], c2[e1], s2[e0], s2[e1])
+// so each 16-byte load yields the two register pairs of an f32x2 operand.
+// Each lane forms mine*cos + partner*(±sin): with the partner negated in
+// the first half of the head that is x cos - y sin, in the second half
+// y cos + x sin -- the same exact products as rotate_one, two at a time.
+
+// The exact path for a whole vector (rare: a result within the interval
+// test's distance of a bf16 rounding boundary, or not finite).
+static __device__ __noinline__ uint4 rotate_vec_packed_exact(uint4 mine, uint4 other, bool first,
+                                                             const float4 *cs, int step)
+{
+    const uint32_t m[4] = {mine.x, mine.y, mine.z, mine.w};
+    const uint32_t o[4] = {other.x, other.y, other.z, other.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 a = cs[(2 * k) * step], b = cs[(2 * k + 1) * step];
+        const uint32_t xw = first ? m[k] : o[k];
+        const uint32_t yw = first ? o[k] : m[k];
+        const uint32_t r0 = rotate_one_exact(xw & 0xFFFFu, yw & 0xFFFFu,
+                                             make_float4(a.x, b.x, a.z, b.z), first, 0.0f);
+        const uint32_t r1 = rotate_one_exact(xw >> 16, yw >> 16,
+                                             make_float4(a.y, b.y, a.w, b.w), first, 0.0f);
+        out[k] = r0 | (r1 << 16);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+__device__ __forceinline__ f2 f2_abs(f2 v) { return v & 0x7FFFFFFF7FFFFFFFull; }
+
+// Rotate one 16-byte vector with f32x2 arithmetic and the same interval
+// test as rotate_one, applied to both elements of a word at once: the ends
+// s ± 2^-21 (|x| + |y|) are rounded as one bf16 pair each; if the pairs
+// agree and are finite the word is the correctly rounded result.
+__device__ __forceinline__ uint4 rotate_vec_packed(uint4 mine, uint4 other, bool first,
+                                                   const float4 *cs, int step)
+{
+    const uint32_t m[4] = {mine.x, mine.y, mine.z, mine.w};
+    const uint32_t o[4] = {other.x, other.y, other.z, other.w};
+    const uint32_t sgn = first ? 0x80008000u : 0u;
+    const f2 kUp = 0x3500000035000000ull;   // (2^-21, 2^-21)
+    const f2 kDn = 0xB5000000B5000000ull;   // (-2^-21, -2^-21)
+    uint32_t out[4], bad = 0u;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 a = cs[(2 * k) * step], b = cs[(2 * k + 1) * step];
+        const f2 c1 = f2_of_bits(__float_as_uint(a.x), __float_as_uint(a.y));
+        const f2 s1 = f2_of_bits(__float_as_uint(a.z), __float_as_uint(a.w));
+        const f2 c2 = f2_of_bits(__float_as_uint(b.x), __float_as_uint(b.y));
+        const f2 s2 = f2_of_bits(__float_as_uint(b.z), __float_as_uint(b.w));
+        const f2 x = f2_of_bf16x2(m[k]);
+        const f2 y = f2_of_bf16x2(o[k] ^ sgn);
+        const f2 t = f2_fma(x, c1, f2_mul(y, s1));   // one rounding of exact products
+        const f2 u = f2_fma(x, c2, f2_mul(y, s2));   // the next 24 bits of cos / sin
+        const f2 s = f2_add(t, u);
+        const f2 mag = f2_add(f2_abs(x), f2_abs(y));
+        const uint32_t hi = bf16x2_rne(f2_fma(mag, kUp, s));
+        const uint32_t lo = bf16x2_rne(f2_fma(mag, kDn, s));
+        // disagreement, or an Inf / NaN half (exponent field all ones)
+        bad |= (hi ^ lo) | (((hi & 0x7FFF7FFFu) + 0x00800080u) & 0x80008000u);
+        out[k] = hi;
+    }
+    if (bad)
+        return rotate_vec_packed_exact(mine, other, first, cs, step);
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
 __device__ __forceinline__ uint4 add_vec(uint4 x, const float *add)
 {
     const uint32_t w[4] = {x.x, x.y, x.z, x.w};

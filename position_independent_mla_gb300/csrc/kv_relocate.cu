@@ -118,9 +118,10 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const
     if (!p.in_place) {
         for (int i = tid; i < G::T * G::kHalf; i += kThreads) {
             const int r = i / G::kHalf, j = i % G::kHalf;
-            s_cs[r][G::cs_index(j)] = (s_src[r] >= 0 && !s_ident[r])
-                                          ? p.table[(int64_t)s_chunk[r] * G::kHalf + j]
-                                          : make_float4(1.f, 0.f, 0.f, 0.f);
+            stage_cs<G, CsOrder<G, PATCH, IL>::kPacked>(
+                s_cs[r], j, (s_src[r] >= 0 && !s_ident[r])
+                                ? p.table[(int64_t)s_chunk[r] * G::kHalf + j]
+                                : make_float4(1.f, 0.f, 0.f, 0.f));
         }
         __syncthreads();
     }

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
         }
     }
     for (int j = tid; j < G::kHalf; j += kThreads)
-        s_cs[G::cs_index(j)] = p.table[(int64_t)q * G::kHalf + j];
+        stage_cs<G, CsOrder<G, false, IL>::kPacked>(s_cs, j, p.table[(int64_t)q * G::kHalf + j]);
     __syncthreads();
 
     const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;
@@ -250,7 +250,8 @@ splice_composed_kernel(const __grid_constant__ ComposedParams p)
     }
     if (tile.unit >= 0)
         for (int j = tid; j < G::kHalf; j += kThreads)
-            s_cs[G::cs_index(j)] = p.table[(int64_t)tile.unit * G::kHalf + j];
+            stage_cs<G, CsOrder<G, false, IL>::kPacked>(s_cs, j,
+                                                     p.table[(int64_t)tile.unit * G::kHalf + j]);
     __syncthreads();
 
     const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(con
     }
     if (down)
         for (int j = tid; j < G::kHalf; j += kThreads)
-            s_cs[G::cs_index(j)] = p.table[(int64_t)q * G::kHalf + j];
+            stage_cs<G, CsOrder<G, false, IL>::kPacked>(s_cs, j, p.table[(int64_t)q * G::kHalf + j]);
     __syncthreads();
 
     const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;

@@ -33,6 +33,19 @@ struct Geo {
     // entries, so the lanes of a warp read them without bank conflicts.
     static constexpr int kCsRow = kHalf + 4;
     static __device__ __forceinline__ int cs_index(int f) { return (f % 8) * HV + f / 8; }
+    // Pair-packed order (rotate_vec_packed): frequency f = 8vv + e feeds
+    // component (e & 1) of the c1/s1 entry (e & ~1)*HV + vv and of the c2/s2
+    // entry (e | 1)*HV + vv -- the same HV*8 entries, regrouped by word.
+    static __device__ __forceinline__ void stage_packed(float4 *row, int f, float4 q)
+    {
+        const int vv = f / 8, e = f % 8, o = e & 1;
+        float *a = reinterpret_cast<float *>(row + (e & ~1) * HV + vv);
+        float *b = reinterpret_cast<float *>(row + (e | 1) * HV + vv);
+        a[o] = q.x;     // c1
+        a[2 + o] = q.z; // s1
+        b[o] = q.y;     // c2
+        b[2 + o] = q.w; // s2
+    }
     static_assert(32 % (2 * HV) == 0, "a rotary head's vectors must tile a warp");
     static_assert(kThreads % (2 * HV) == 0, "partner lanes must stay in one item round");
 };
@@ -45,6 +58,25 @@ using GeoGqa = Geo<kTileGqa, 128, 8, 8, 2>;
 using GeoGqa4 = Geo<kTileGqa4, 64, 4, 8, 2>;
 // MHA rows: V 32x128 + K 32x128 (Llama-2-7B shape).
 using GeoMha = Geo<kTileMha, 512, 32, 8, 2>;
+
+// Multi-head rows (GQA, MHA: rotation is half of every row) without a
+// patch term, in rotate-half pairing, take the pair-packed rotation; the
+// others (MLA's single 64-wide head, patched or interleaved rows) keep one
+// (c1, c2, s1, s2) entry per frequency.
+template <class G, bool PATCH, bool IL>
+struct CsOrder {
+    static constexpr bool kPacked = !PATCH && !IL && G::NH > 1;
+};
+
+// Write table entry q of frequency f into a shared-memory cos/sin row.
+template <class G, bool PACKED>
+__device__ __forceinline__ void stage_cs(float4 *row, int f, float4 q)
+{
+    if (PACKED)
+        G::stage_packed(row, f, q);
+    else
+        row[G::cs_index(f)] = q;
+}
 
 template <class G>
 struct GeoTag {
@@ -250,6 +282,9 @@ __device__ __forceinline__ void store_tile(const RowsAt &at, const int64_t *idx,
                     out = patched ? add_vec(regs.r[k], add) : regs.r[k];
                 else if (IL)
                     out = rotate_vec_il<G>(regs.r[k], cs + row * cs_row_stride, v, add);
+                else if (CsOrder<G, PATCH, IL>::kPacked)
+                    out = rotate_vec_packed(regs.r[k], partner, first,
+                                            cs + row * cs_row_stride + fb / 8, G::HV);
                 else
                     out = rotate_vec(regs.r[k], partner, first,
                                      cs + row * cs_row_stride + fb / 8, G::HV, add);

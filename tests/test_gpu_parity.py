@@ -197,19 +197,31 @@ def test_relocate_reports_a_bad_index_and_skips_its_row(orc):
     check_pool(dst, "relocate with one bad index")
 
 
-def test_relocate_nonfinite_inputs(orc):
-    wl, src, dst, dev = _reloc_case("mla", 260, num_reqs=1, chunks=2, lo=40, hi=60,
+@pytest.mark.parametrize("shape", ["mla", "gqa"])
+def test_relocate_nonfinite_inputs(orc, shape):
+    wl, src, dst, dev = _reloc_case(shape, 260, num_reqs=1, chunks=2, lo=40, hi=60,
                                     deltas=[321, -77])
-    # plant Inf / NaN in a few source k_pe values (and their bf16 mirrors)
+
+    def plant(s, cols, b):
+        src.orc.rot[0, s, cols] = b
+        src.rot_view[0, s, cols] = torch.tensor(int(np.array(b, np.uint16).view(np.int16)),
+                                                dtype=torch.int16).view(torch.bfloat16)
+
+    # Inf / NaN in a few source rotary values (and their bf16 mirrors)
     specials = [0x7F80, 0xFF80, 0x7FC0, 0x7F81]
     for k, b in enumerate(specials):
-        s = int(wl.src_slots[k])
-        src.orc.rot[0, s, 3 + k] = b
-        src.rot_view[0, s, 3 + k] = torch.tensor(int(np.array(b, np.uint16).view(np.int16)),
-                                                 dtype=torch.int16).view(torch.bfloat16)
+        plant(int(wl.src_slots[k]), 3 + 17 * k, b)
+    # a whole half-head at +Inf, and the largest finite bf16 (0x7F7F) in both
+    # halves of a head, with equal and opposite signs: the rotated value
+    # overflows fp32 for some frequencies, the rounding gives +-Inf
+    h = src.d // 2
+    plant(int(wl.src_slots[4]), slice(0, h), 0x7F80)
+    plant(int(wl.src_slots[5]), slice(0, src.d), 0x7F7F)
+    plant(int(wl.src_slots[6]), slice(0, h), 0x7F7F)
+    plant(int(wl.src_slots[6]), slice(h, src.d), 0xFF7F)
     assert _run_relocate(wl, src, dst, dev) == kv.KV_OK
     _oracle_relocate(orc, wl, src, dst)
-    check_pool(dst, "relocate with Inf/NaN")
+    check_pool(dst, "relocate with Inf/NaN and overflow")
 
 
 @pytest.mark.parametrize("shape", ["mla", "gqa"])

@@ -151,6 +151,19 @@ static __device__ __noinline__ uint32_t rotate_one_exact(uint32_t xb, uint32_t y
         }
         float t, et;
         two_sum(p, q, t, et);
+        if (fabsf(t) > 3.40282347e38f) {
+            // x*c1 + y*s1 reaches the fp32 overflow threshold (inputs near
+            // bf16's largest value): redo at half scale -- exact, the
+            // operands are far from the subnormal range -- and double the
+            // rounded result; beyond bf16's largest finite value the
+            // doubling gives Inf, as rounding the fp64 value does.
+            two_sum(0.5f * p, 0.5f * q, t, et);
+            two_sum(t, et + 0.5f * u, hi, lo);
+            float s, e;
+            two_sum(hi, lo + 0.5f * add, s, e);
+            const uint32_t r = bf16_round(s, e);
+            return ((r & 0x7F80u) == 0x7F00u) ? ((r & 0x8000u) | 0x7F80u) : r + 0x80u;
+        }
         two_sum(t, et + u, hi, lo);
     } else {
         // Inf / NaN inputs: plain IEEE arithmetic, as the fp64 definition does
@@ -269,26 +282,19 @@ __device__ __forceinline__ uint4 rotate_vec(uint4 mine, uint4 other, bool first,
 // the first half of the head that is x cos - y sin, in the second half
 // y cos + x sin -- the same exact products as rotate_one, two at a time.
 
-// The exact path for a whole vector (rare: a result within the interval
-// test's distance of a bf16 rounding boundary, or not finite).
-static __device__ __noinline__ uint4 rotate_vec_packed_exact(uint4 mine, uint4 other, bool first,
-                                                             const float4 *cs, int step)
+// The exact path for one word (rare: a result within the interval test's
+// distance of a bf16 rounding boundary, or not finite).  a, b are the word's
+// two table entries; mw, ow this lane's and the partner's words.
+static __device__ __noinline__ uint32_t rotate_word_exact(uint32_t mw, uint32_t ow, bool first,
+                                                          float4 a, float4 b)
 {
-    const uint32_t m[4] = {mine.x, mine.y, mine.z, mine.w};
-    const uint32_t o[4] = {other.x, other.y, other.z, other.w};
-    uint32_t out[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float4 a = cs[(2 * k) * step], b = cs[(2 * k + 1) * step];
-        const uint32_t xw = first ? m[k] : o[k];
-        const uint32_t yw = first ? o[k] : m[k];
-        const uint32_t r0 = rotate_one_exact(xw & 0xFFFFu, yw & 0xFFFFu,
-                                             make_float4(a.x, b.x, a.z, b.z), first, 0.0f);
-        const uint32_t r1 = rotate_one_exact(xw >> 16, yw >> 16,
-                                             make_float4(a.y, b.y, a.w, b.w), first, 0.0f);
-        out[k] = r0 | (r1 << 16);
-    }
-    return make_uint4(out[0], out[1], out[2], out[3]);
+    const uint32_t xw = first ? mw : ow;
+    const uint32_t yw = first ? ow : mw;
+    const uint32_t r0 = rotate_one_exact(xw & 0xFFFFu, yw & 0xFFFFu,
+                                         make_float4(a.x, b.x, a.z, b.z), first, 0.0f);
+    const uint32_t r1 = rotate_one_exact(xw >> 16, yw >> 16,
+                                         make_float4(a.y, b.y, a.w, b.w), first, 0.0f);
+    return r0 | (r1 << 16);
 }
 
 __device__ __forceinline__ f2 f2_abs(f2 v) { return v & 0x7FFFFFFF7FFFFFFFull; }
@@ -305,7 +311,7 @@ __device__ __forceinline__ uint4 rotate_vec_packed(uint4 mine, uint4 other, bool
     const uint32_t sgn = first ? 0x80008000u : 0u;
     const f2 kUp = 0x3500000035000000ull;   // (2^-21, 2^-21)
     const f2 kDn = 0xB5000000B5000000ull;   // (-2^-21, -2^-21)
-    uint32_t out[4], bad = 0u;
+    uint32_t out[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const float4 a = cs[(2 * k) * step], b = cs[(2 * k + 1) * step];
@@ -322,11 +328,9 @@ __device__ __forceinline__ uint4 rotate_vec_packed(uint4 mine, uint4 other, bool
         const uint32_t hi = bf16x2_rne(f2_fma(mag, kUp, s));
         const uint32_t lo = bf16x2_rne(f2_fma(mag, kDn, s));
         // disagreement, or an Inf / NaN half (exponent field all ones)
-        bad |= (hi ^ lo) | (((hi & 0x7FFF7FFFu) + 0x00800080u) & 0x80008000u);
-        out[k] = hi;
+        const uint32_t bad = (hi ^ lo) | (((hi & 0x7FFF7FFFu) + 0x00800080u) & 0x80008000u);
+        out[k] = bad ? rotate_word_exact(m[k], o[k], first, a, b) : hi;
     }
-    if (bad)
-        return rotate_vec_packed_exact(mine, other, first, cs, step);
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 

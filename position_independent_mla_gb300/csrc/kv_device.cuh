@@ -176,11 +176,12 @@ static __device__ __noinline__ uint32_t rotate_one_exact(uint32_t xb, uint32_t y
     return bf16_round(s, e);
 }
 
-// Same result, cheaply: with exact leading products, t + (u + add) is the
-// rotated value to within 2^-23 (|x| + |y| + |add|), so its round-to-nearest-
-// even is already the correctly rounded bf16 unless a bf16 rounding boundary
-// lies within that distance (the interval test below), or it is not finite.
-// Those rare cases (about 2e-4 of values) take the exact path.
+// Same result, cheaply: with exact leading products (inputs above fp32's
+// subnormal range), t + (u + add) is the rotated value to within about
+// 2^-23 (|x| + |y| + |add|), so its round-to-nearest-even is already the
+// correctly rounded bf16 unless a bf16 rounding boundary lies near it (the
+// interval test below), or it is not finite.  Those rare cases (about one
+// value in 10^4) take the exact path.
 __device__ __forceinline__ uint32_t rotate_one(uint32_t xb, uint32_t yb, float4 cs, bool first,
                                                float add)
 {
@@ -194,10 +195,13 @@ __device__ __forceinline__ uint32_t rotate_one(uint32_t xb, uint32_t yb, float4 
         u = fmaf(x, cs.w, y * cs.y);
     }
     const float s = t + (u + add);
-    // s is within 2^-23 (|x| + |y| + |add|) of the exact value; round both ends
-    // of an interval twice as wide: if they agree, the exact value rounds to
-    // the same bf16 (rounding is monotone).  This also covers cancellation.
-    const float r = 4.76837158203125e-7f * (fabsf(x) + fabsf(y) + fabsf(add)); // 2^-21
+    // s is within 2^-23 (|x| + |y| + |add|)(1 + 2^-15) of the exact value
+    // (two roundings of terms no larger than |x| + |y| + |add|, plus the
+    // small c2/s2 terms); the ends s +- 2^-22 (|x| + |y| + |add|) lie beyond
+    // that distance even after their own rounding, so if both ends round to
+    // the same bf16, so does the exact value (rounding is monotone).  This
+    // also covers cancellation.
+    const float r = 2.384185791015625e-7f * (fabsf(x) + fabsf(y) + fabsf(add)); // 2^-22
     uint32_t ends;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(ends) : "f"(s + r), "f"(s - r));
     if (((ends ^ (ends >> 16)) & 0xFFFFu) != 0u || !(fabsf(s) <= 3.40282347e38f))
@@ -282,11 +286,10 @@ __device__ __forceinline__ uint4 rotate_vec(uint4 mine, uint4 other, bool first,
 // the first half of the head that is x cos - y sin, in the second half
 // y cos + x sin -- the same exact products as rotate_one, two at a time.
 
-// The exact path for one word (rare: a result within the interval test's
-// distance of a bf16 rounding boundary, or not finite).  a, b are the word's
-// two table entries; mw, ow this lane's and the partner's words.
-static __device__ __noinline__ uint32_t rotate_word_exact(uint32_t mw, uint32_t ow, bool first,
-                                                          float4 a, float4 b)
+// The exact path for one word.  a, b are the word's two table entries; mw,
+// ow this lane's and the partner's words.
+__device__ __forceinline__ uint32_t rotate_word_exact(uint32_t mw, uint32_t ow, bool first,
+                                                      float4 a, float4 b)
 {
     const uint32_t xw = first ? mw : ow;
     const uint32_t yw = first ? ow : mw;
@@ -297,21 +300,40 @@ static __device__ __noinline__ uint32_t rotate_word_exact(uint32_t mw, uint32_t 
     return r0 | (r1 << 16);
 }
 
+// Redo the words of a vector whose fast results failed the interval test
+// (rare: a result within the test's distance of a bf16 rounding boundary, or
+// not finite); `bad` is nonzero for those words.
+static __device__ __noinline__ uint4 fix_vec_packed(uint4 out, uint4 bad, uint4 mine, uint4 other,
+                                                    bool first, const float4 *cs, int step)
+{
+    uint32_t r[4] = {out.x, out.y, out.z, out.w};
+    const uint32_t b[4] = {bad.x, bad.y, bad.z, bad.w};
+    const uint32_t m[4] = {mine.x, mine.y, mine.z, mine.w};
+    const uint32_t o[4] = {other.x, other.y, other.z, other.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (b[k])
+            r[k] = rotate_word_exact(m[k], o[k], first, cs[(2 * k) * step],
+                                     cs[(2 * k + 1) * step]);
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 __device__ __forceinline__ f2 f2_abs(f2 v) { return v & 0x7FFFFFFF7FFFFFFFull; }
 
 // Rotate one 16-byte vector with f32x2 arithmetic and the same interval
 // test as rotate_one, applied to both elements of a word at once: the ends
-// s ± 2^-21 (|x| + |y|) are rounded as one bf16 pair each; if the pairs
-// agree and are finite the word is the correctly rounded result.
+// s ± 2^-22 (|x| + |y|) are rounded as one bf16 pair each; if the pairs
+// agree and are finite the word is the correctly rounded result.  One branch
+// per vector, so the four words' arithmetic interleaves.
 __device__ __forceinline__ uint4 rotate_vec_packed(uint4 mine, uint4 other, bool first,
                                                    const float4 *cs, int step)
 {
     const uint32_t m[4] = {mine.x, mine.y, mine.z, mine.w};
     const uint32_t o[4] = {other.x, other.y, other.z, other.w};
     const uint32_t sgn = first ? 0x80008000u : 0u;
-    const f2 kUp = 0x3500000035000000ull;   // (2^-21, 2^-21)
-    const f2 kDn = 0xB5000000B5000000ull;   // (-2^-21, -2^-21)
-    uint32_t out[4];
+    const f2 kUp = 0x3480000034800000ull;   // (2^-22, 2^-22)
+    const f2 kDn = 0xB4800000B4800000ull;   // (-2^-22, -2^-22)
+    uint32_t out[4], bad[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const float4 a = cs[(2 * k) * step], b = cs[(2 * k + 1) * step];
@@ -328,10 +350,14 @@ __device__ __forceinline__ uint4 rotate_vec_packed(uint4 mine, uint4 other, bool
         const uint32_t hi = bf16x2_rne(f2_fma(mag, kUp, s));
         const uint32_t lo = bf16x2_rne(f2_fma(mag, kDn, s));
         // disagreement, or an Inf / NaN half (exponent field all ones)
-        const uint32_t bad = (hi ^ lo) | (((hi & 0x7FFF7FFFu) + 0x00800080u) & 0x80008000u);
-        out[k] = bad ? rotate_word_exact(m[k], o[k], first, a, b) : hi;
+        bad[k] = (hi ^ lo) | (((hi & 0x7FFF7FFFu) + 0x00800080u) & 0x80008000u);
+        out[k] = hi;
     }
-    return make_uint4(out[0], out[1], out[2], out[3]);
+    const uint4 res = make_uint4(out[0], out[1], out[2], out[3]);
+    if ((bad[0] | bad[1]) | (bad[2] | bad[3]))
+        return fix_vec_packed(res, make_uint4(bad[0], bad[1], bad[2], bad[3]), mine, other, first,
+                              cs, step);
+    return res;
 }
 
 __device__ __forceinline__ uint4 add_vec(uint4 x, const float *add)

@@ -169,6 +169,16 @@ class Oracle:
         lib.kvo_splice_composed.restype = i32
         lib.kvo_splice_composed.argtypes = [C.POINTER(_Pool), i32, i32, vp, i32, vp, vp, vp, vp,
                                             vp, vp]
+        u64 = C.c_uint64
+        lib.kvo_splitmix64_at.restype = u64
+        lib.kvo_splitmix64_at.argtypes = [u64, u64]
+        lib.kvo_xxh64.restype = u64
+        lib.kvo_xxh64.argtypes = [vp, i64, u64]
+        lib.kvo_gear_hashes.argtypes = [vp, i64, u64, vp]
+        lib.kvo_cdc.restype = i64
+        lib.kvo_cdc.argtypes = [i32, vp, vp, u64, u64, u64, i64, vp, vp]
+        lib.kvo_fingerprint.restype = i32
+        lib.kvo_fingerprint.argtypes = [i64, vp, vp, vp, u64, vp]
 
     # -- scalar / vector helpers ------------------------------------------
     def round_bf16(self, v: float) -> int:
@@ -265,6 +275,47 @@ class Oracle:
         return int(self._lib.kvo_splice_composed(
             C.byref(pp), len(seq_lens), s_start.shape[0], _ptr(bt), bt.shape[1], _ptr(seq_lens),
             _ptr(s_start), _ptr(s_end), _ptr(stub_len), _ptr(stub_copy), _ptr(stub_rot)))
+
+
+    # -- content-defined chunking (Irminsul §2.2) ---------------------------
+    def splitmix64_at(self, seed: int, n: int) -> int:
+        return int(self._lib.kvo_splitmix64_at(seed & (2**64 - 1), n & (2**64 - 1)))
+
+    def xxh64(self, data: bytes, seed: int = 0) -> int:
+        buf = C.create_string_buffer(bytes(data), max(1, len(data)))
+        return int(self._lib.kvo_xxh64(C.cast(buf, C.c_void_p), len(data), seed & (2**64 - 1)))
+
+    def gear_hashes(self, tokens, gear_seed: int) -> np.ndarray:
+        t = _i32(tokens)
+        h = np.empty(len(t), dtype=np.uint64)
+        self._lib.kvo_gear_hashes(_ptr(t), len(t), gear_seed & (2**64 - 1), _ptr(h))
+        return h
+
+    def cdc(self, stream_off, tokens, gear_seed: int, threshold: int, fp_seed: int = 0,
+            max_chunks: Optional[int] = None):
+        """(chunk_end int64, fingerprint uint64, count): every stream's chunks in order."""
+        off = np.ascontiguousarray(np.asarray(stream_off, dtype=np.int64))
+        t = _i32(tokens)
+        cap = len(t) if max_chunks is None else int(max_chunks)
+        ends = np.zeros(max(cap, 1), dtype=np.int64)
+        fps = np.zeros(max(cap, 1), dtype=np.uint64)
+        n = int(self._lib.kvo_cdc(len(off) - 1, _ptr(off), _ptr(t), gear_seed & (2**64 - 1),
+                                  threshold & (2**64 - 1), fp_seed & (2**64 - 1), cap,
+                                  _ptr(ends), _ptr(fps)))
+        if n < 0:
+            raise ValueError("malformed stream offsets")
+        k = min(n, cap)
+        return ends[:k], fps[:k], n
+
+    def fingerprint(self, starts, ends, tokens, fp_seed: int = 0) -> np.ndarray:
+        a = np.ascontiguousarray(np.asarray(starts, dtype=np.int64))
+        b = np.ascontiguousarray(np.asarray(ends, dtype=np.int64))
+        t = _i32(tokens)
+        out = np.zeros(max(len(a), 1), dtype=np.uint64)
+        if self._lib.kvo_fingerprint(len(a), _ptr(a), _ptr(b), _ptr(t), fp_seed & (2**64 - 1),
+                                     _ptr(out)) != 0:
+            raise ValueError("bad token range")
+        return out[:len(a)]
 
 
 _default: Optional[Oracle] = None

@@ -670,3 +670,193 @@ int kvo_splice_composed(kvo_pool *pool, int num_seqs, int num_dirs, const int32_
     }
     return KVO_OK;
 }
+
+/* ------------------------------------------------------------------ */
+/* Content-defined chunking of token streams                           */
+/* ------------------------------------------------------------------ */
+/*
+ * Irminsul §2.2 ("content hash keying with CDC"): the registry is keyed by
+ * content.  A Gear rolling hash over windows of 64 tokens ends a chunk
+ * where the hash falls below a threshold, so chunk boundaries follow the
+ * content and not its offset; each chunk is named by its xxHash64
+ * fingerprint.  The fixed-window fallback (S1) fingerprints windows of 128
+ * tokens instead.  The pages fix neither the Gear table nor the threshold.
+ * Readings used here and nowhere else:
+ *   - the Gear value of token id x is output number x (from 0) of the
+ *     SplitMix64 generator (Steele, Lea and Flood, OOPSLA 2014) seeded with
+ *     gear_seed: the generator's state after x + 1 steps of the golden-ratio
+ *     increment, passed through its finalising mix;
+ *   - h(-1) = 0 at the start of every stream and h(i) = 2 h(i-1) + G(x_i)
+ *     modulo 2^64, so h(i) holds the last 64 tokens (older ones are shifted
+ *     out) -- the 64-token window;
+ *   - a chunk ends after token i when h(i) < threshold, and at the end of
+ *     its stream; an empty stream has no chunk;
+ *   - a chunk's fingerprint is XXH64 (Collet's published algorithm) of its
+ *     token ids as 4-byte little-endian words, seeded with fp_seed.
+ */
+
+static uint64_t rotl64(uint64_t v, int r) { return (v << r) | (v >> (64 - r)); }
+
+/* output number n (from 0) of SplitMix64 seeded with `seed` */
+uint64_t kvo_splitmix64_at(uint64_t seed, uint64_t n)
+{
+    uint64_t z = seed + (n + 1u) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* The five primes of XXH64. */
+#define XXP1 0x9E3779B185EBCA87ull
+#define XXP2 0xC2B2AE3D27D4EB4Full
+#define XXP3 0x165667B19E3779F9ull
+#define XXP4 0x85EBCA77C2B2AE63ull
+#define XXP5 0x27D4EB2F165667C5ull
+
+static uint64_t le64(const uint8_t *p)
+{
+    uint64_t v = 0;
+    for (int i = 7; i >= 0; --i)
+        v = (v << 8) | p[i];
+    return v;
+}
+
+static uint32_t le32(const uint8_t *p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) |
+           ((uint32_t)p[3] << 24);
+}
+
+/* one accumulator step: fold an 8-byte lane into acc */
+static uint64_t xx_round(uint64_t acc, uint64_t lane)
+{
+    acc += lane * XXP2;
+    acc = rotl64(acc, 31);
+    return acc * XXP1;
+}
+
+static uint64_t xx_merge(uint64_t acc, uint64_t v)
+{
+    acc ^= xx_round(0, v);
+    return acc * XXP1 + XXP4;
+}
+
+/* XXH64 of `len` bytes: 32-byte stripes into four accumulators, then the
+ * remaining 8-, 4- and 1-byte pieces, then the final avalanche. */
+uint64_t kvo_xxh64(const void *data, int64_t len, uint64_t seed)
+{
+    const uint8_t *p = (const uint8_t *)data;
+    const uint8_t *end = p + len;
+    uint64_t acc;
+    if (len >= 32) {
+        uint64_t v1 = seed + XXP1 + XXP2, v2 = seed + XXP2, v3 = seed, v4 = seed - XXP1;
+        while (end - p >= 32) {
+            v1 = xx_round(v1, le64(p));
+            v2 = xx_round(v2, le64(p + 8));
+            v3 = xx_round(v3, le64(p + 16));
+            v4 = xx_round(v4, le64(p + 24));
+            p += 32;
+        }
+        acc = rotl64(v1, 1) + rotl64(v2, 7) + rotl64(v3, 12) + rotl64(v4, 18);
+        acc = xx_merge(acc, v1);
+        acc = xx_merge(acc, v2);
+        acc = xx_merge(acc, v3);
+        acc = xx_merge(acc, v4);
+    } else {
+        acc = seed + XXP5;
+    }
+    acc += (uint64_t)len;
+    while (end - p >= 8) {
+        acc ^= xx_round(0, le64(p));
+        acc = rotl64(acc, 27) * XXP1 + XXP4;
+        p += 8;
+    }
+    if (end - p >= 4) {
+        acc ^= (uint64_t)le32(p) * XXP1;
+        acc = rotl64(acc, 23) * XXP2 + XXP3;
+        p += 4;
+    }
+    while (p < end) {
+        acc ^= (uint64_t)(*p) * XXP5;
+        acc = rotl64(acc, 11) * XXP1;
+        ++p;
+    }
+    acc ^= acc >> 33;
+    acc *= XXP2;
+    acc ^= acc >> 29;
+    acc *= XXP3;
+    acc ^= acc >> 32;
+    return acc;
+}
+
+/* XXH64 of tokens[0..n) as 4-byte little-endian words */
+static uint64_t tokens_xxh64(const int32_t *tokens, int64_t n, uint64_t seed)
+{
+    uint8_t *buf = (uint8_t *)malloc((size_t)(n > 0 ? n : 1) * 4);
+    for (int64_t i = 0; i < n; ++i) {
+        const uint32_t v = (uint32_t)tokens[i];
+        buf[4 * i] = (uint8_t)v;
+        buf[4 * i + 1] = (uint8_t)(v >> 8);
+        buf[4 * i + 2] = (uint8_t)(v >> 16);
+        buf[4 * i + 3] = (uint8_t)(v >> 24);
+    }
+    const uint64_t h = kvo_xxh64(buf, n * 4, seed);
+    free(buf);
+    return h;
+}
+
+/* The Gear hash h(i) after every token of one stream. */
+void kvo_gear_hashes(const int32_t *tokens, int64_t n, uint64_t gear_seed, uint64_t *h)
+{
+    uint64_t acc = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        acc = 2u * acc + kvo_splitmix64_at(gear_seed, (uint64_t)(uint32_t)tokens[i]);
+        h[i] = acc;
+    }
+}
+
+/* Chunks of every stream: chunk_end[k] (exclusive end, a global token
+ * offset) and fingerprint[k], in stream order.  Stream s is tokens
+ * [stream_off[s], stream_off[s+1]).  Returns the number of chunks; when it
+ * exceeds max_chunks only the first max_chunks are written.  Returns -1 on
+ * malformed offsets. */
+int64_t kvo_cdc(int num_streams, const int64_t *stream_off, const int32_t *tokens,
+                uint64_t gear_seed, uint64_t threshold, uint64_t fp_seed, int64_t max_chunks,
+                int64_t *chunk_end, uint64_t *fingerprint)
+{
+    if (num_streams < 0 || (num_streams > 0 && stream_off[0] != 0))
+        return -1;
+    int64_t count = 0;
+    for (int s = 0; s < num_streams; ++s) {
+        const int64_t a = stream_off[s], b = stream_off[s + 1];
+        if (b < a)
+            return -1;
+        uint64_t acc = 0;
+        int64_t start = a;
+        for (int64_t i = a; i < b; ++i) {
+            acc = 2u * acc + kvo_splitmix64_at(gear_seed, (uint64_t)(uint32_t)tokens[i]);
+            if (acc < threshold || i == b - 1) {
+                if (count < max_chunks) {
+                    chunk_end[count] = i + 1;
+                    fingerprint[count] = tokens_xxh64(tokens + start, i + 1 - start, fp_seed);
+                }
+                ++count;
+                start = i + 1;
+            }
+        }
+    }
+    return count;
+}
+
+/* Fingerprints of arbitrary token ranges [start[k], end[k]) (the fixed-window
+ * fallback passes consecutive 128-token windows).  Returns -1 on a bad range. */
+int kvo_fingerprint(int64_t num_ranges, const int64_t *start, const int64_t *end,
+                    const int32_t *tokens, uint64_t fp_seed, uint64_t *fingerprint)
+{
+    for (int64_t k = 0; k < num_ranges; ++k) {
+        if (end[k] < start[k] || start[k] < 0)
+            return -1;
+        fingerprint[k] = tokens_xxh64(tokens + start[k], end[k] - start[k], fp_seed);
+    }
+    return 0;
+}

@@ -243,3 +243,37 @@ def shard(n: int, rank: int, world: int) -> range:
     base, extra = divmod(n, world)
     lo = rank * base + min(rank, extra)
     return range(lo, lo + base + (1 if rank < extra else 0))
+
+
+@dataclass
+class TokenStreams:
+    stream_off: np.ndarray  # int64 [num_streams + 1], prefix offsets from 0
+    tokens: np.ndarray      # int32 [total], token ids
+
+    @property
+    def num_streams(self) -> int:
+        return len(self.stream_off) - 1
+
+
+def token_streams(seed: int, lengths, vocab: int = 129280, shared_segments: int = 0,
+                  segment_lo: int = 512, segment_hi: int = 4096) -> TokenStreams:
+    """Token-id streams of the given lengths, ids U[0, vocab).  With
+    `shared_segments` > 0, each stream also carries copies of segments drawn
+    from a common pool, pasted at random offsets, so equal content recurs at
+    shifted positions (the agentic traffic a content-keyed cache serves)."""
+    rng = np.random.default_rng(seed)
+    lengths = np.asarray(lengths, dtype=np.int64)
+    off = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    tokens = rng.integers(0, vocab, int(off[-1]), dtype=np.int64).astype(np.int32)
+    if shared_segments > 0:
+        pool = [rng.integers(0, vocab, int(rng.integers(segment_lo, segment_hi + 1)),
+                             dtype=np.int64).astype(np.int32) for _ in range(shared_segments)]
+        for s in range(len(lengths)):
+            n = int(lengths[s])
+            for _ in range(3):
+                seg = pool[int(rng.integers(len(pool)))]
+                if len(seg) >= n:
+                    continue
+                at = int(rng.integers(0, n - len(seg) + 1))
+                tokens[off[s] + at: off[s] + at + len(seg)] = seg
+    return TokenStreams(off, tokens)

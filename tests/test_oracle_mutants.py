@@ -13,6 +13,7 @@ import pytest
 
 import oracle as O
 from oracle import build as obuild
+import test_oracle_cdc_pins as CDC
 import test_oracle_pins as P
 
 SRC = os.path.join(os.path.dirname(obuild.__file__), "kvoracle.c")
@@ -50,6 +51,19 @@ MUTANTS = [
     ("composed-origin-position-zero", "cur[p].written = p;", "cur[p].written = 0;", 0),
     ("composed-stub-never-rotated", "rd, p - cur[p].written,", "rd, cur[p].src >= 0 ? p - cur[p].written : 0,", 0),
     ("composed-stub-rows-ignore-sequence", "if (i2 < i || (i2 == i && q2 < q))", "if (i2 < i)", 0),
+    ("xxh-round-rotation", "acc = rotl64(acc, 31);", "acc = rotl64(acc, 33);", 0),
+    ("xxh-prime", "#define XXP2 0xC2B2AE3D27D4EB4Full", "#define XXP2 0xC2B2AE3D27D4EB4Dull", 0),
+    ("xxh-four-byte-tail", "acc = rotl64(acc, 23) * XXP2 + XXP3;", "acc = rotl64(acc, 21) * XXP2 + XXP3;", 0),
+    ("xxh-no-length", "acc += (uint64_t)len;", "acc += 0;", 0),
+    ("splitmix-counter-offset", "seed + (n + 1u) * 0x9E3779B97F4A7C15ull", "seed + n * 0x9E3779B97F4A7C15ull", 0),
+    ("gear-no-shift", "acc = 2u * acc + kvo_splitmix64_at", "acc = acc + kvo_splitmix64_at", 1),
+    ("gear-window-sum-no-shift", "acc = 2u * acc + kvo_splitmix64_at", "acc = acc + kvo_splitmix64_at", 0),
+    ("cdc-threshold-flipped", "if (acc < threshold || i == b - 1)", "if (acc > threshold || i == b - 1)", 0),
+    ("cdc-hash-not-reset-per-stream", "        uint64_t acc = 0;\n        int64_t start = a;",
+     "        static uint64_t acc = 0;\n        int64_t start = a;", 0),
+    ("fingerprint-from-stream-start", "tokens_xxh64(tokens + start, i + 1 - start, fp_seed)",
+     "tokens_xxh64(tokens + a, i + 1 - a, fp_seed)", 0),
+    ("token-bytes-big-endian", "buf[4 * i] = (uint8_t)v;", "buf[4 * i] = (uint8_t)(v >> 24);", 0),
 ]
 
 
@@ -81,6 +95,14 @@ def _pins():
         ("composed-single", P.test_composed_single_directive_is_the_splice),
         ("composed-batch", P.test_composed_three_directives_batch_gqa),
         ("composed-brute", P.test_composed_brute_force_two_directives),
+        ("xxh64-empty", CDC.test_xxh64_published_empty_input_value),
+        ("splitmix64-outputs", CDC.test_splitmix64_published_first_outputs),
+        ("xxh64-library", CDC.test_xxh64_matches_the_installed_library),
+        ("gear-window", CDC.test_gear_hash_is_the_64_token_window_sum),
+        ("cdc-tiling", CDC.test_chunks_tile_each_stream_and_fingerprints_name_their_tokens),
+        ("cdc-content", CDC.test_chunk_ends_follow_content_not_offset),
+        ("cdc-mean-length", CDC.test_threshold_sets_the_mean_chunk_length),
+        ("cdc-extremes", CDC.test_threshold_extremes_and_capacity),
     ]
 
 

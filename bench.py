@@ -70,6 +70,7 @@ KERNEL_SOURCES = {
     "splice_mla_128k_composed": ("kv_splice.cu",) + _COMMON_SOURCES,
     "splice_mla_128k_remap": ("kv_splice.cu",) + _COMMON_SOURCES,
     "window_gqa": ("kv_splice.cu", "kv_patch_tc.cu") + _COMMON_SOURCES,
+    "cdc_tokens": ("kv_cdc.cu",) + _COMMON_SOURCES,
 }
 
 
@@ -1794,12 +1795,141 @@ def run_sweep_mla(args, rank, world, local):
     }
 
 
+# ---------------------------------------------------------------------------
+# Workload: Irminsul content-defined chunking of token streams
+# ---------------------------------------------------------------------------
+
+CDC_TOKENS = dict(num_streams=384, stream_len=131072, vocab=129280, shared_segments=64,
+                  log_mean=8, gear_seed=0x1F2E3D4C5B6A7988, fp_seed=0)
+# A small case of the same kernels (16 MB of tokens).
+CDC_TOKENS_SMALL = dict(CDC_TOKENS, num_streams=32)
+
+
+def build_cdc(rank: int, cfg, device: str = "cuda"):
+    import position_independent_mla_gb300 as kv
+
+    ts = synth.token_streams(5005 + 100 * rank, [cfg["stream_len"]] * cfg["num_streams"],
+                             vocab=cfg["vocab"], shared_segments=cfg["shared_segments"])
+    total = len(ts.tokens)
+    host = {"off": torch.from_numpy(ts.stream_off).pin_memory(),
+            "tok": torch.from_numpy(ts.tokens).pin_memory()}
+    dev = {k: v.to(device) for k, v in host.items()}
+    out = dict(ends=torch.empty(total, dtype=torch.int64, device=device),
+               fps=torch.empty(total, dtype=torch.int64, device=device),
+               cnt=torch.zeros(1, dtype=torch.int64, device=device))
+    ws = torch.empty(kv.kv_cdc_workspace_size(total), dtype=torch.uint8, device=device)
+    return dict(ts=ts, host=host, dev=dev, ws=ws, total=total, cfg=cfg,
+                threshold=1 << (64 - cfg["log_mean"]), **out)
+
+
+def cdc_call(st, dev=None, stream=None):
+    import position_independent_mla_gb300 as kv
+
+    d, c = dev if dev is not None else st["dev"], st["cfg"]
+    kv.kv_cdc(st["ts"].num_streams, d["off"], st["total"], d["tok"], c["gear_seed"],
+              st["threshold"], c["fp_seed"], st["total"], st["ends"], st["fps"], st["cnt"],
+              st["ws"], stream=stream)
+    return kv.kv_last_launch_count()
+
+
+def check_cdc(st, orc) -> dict:
+    """Full parity: every chunk end and fingerprint of the last call against
+    the oracle run on the same streams."""
+    c = st["cfg"]
+    w_ends, w_fps, w_n = orc.cdc(st["ts"].stream_off, st["ts"].tokens, c["gear_seed"],
+                                 st["threshold"], c["fp_seed"])
+    n = int(st["cnt"].item())
+    ends = st["ends"][:n].cpu().numpy()
+    fps = st["fps"][:n].cpu().numpy().view(np.uint64)
+    same = n == w_n
+    return {"chunks": n, "oracle_chunks": int(w_n),
+            "ends_differing": int(np.sum(ends != w_ends)) if same else n,
+            "fingerprints_differing": int(np.sum(fps != w_fps)) if same else n}
+
+
+def run_cdc_tokens(args, rank, world, local):
+    """Content-defined chunking of agentic token streams (Irminsul §2.2): every
+    stream cut where its 64-token Gear hash falls below the threshold, every
+    chunk fingerprinted with XXH64 -- four kernels per call."""
+    import position_independent_mla_gb300 as kv
+
+    cfg = CDC_TOKENS_SMALL if args.small else CDC_TOKENS
+    st = build_cdc(rank, cfg)
+    K, W = args.steps, args.warmup
+    total = st["total"]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    ms, kms, launches = _timed(lambda: cdc_call(st), K, W)
+    assert kv.kv_get_device_status(st["ws"]) == kv.KV_OK
+    n_chunks = int(st["cnt"].item())
+    # end to end: pinned host tokens and offsets in, the chunk count back
+    host, dev = st["host"], st["dev"]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        cdc_call(st, dev)
+        n_back = int(st["cnt"].item())
+        assert kv.kv_get_device_status(st["ws"], stream) == kv.KV_OK
+    e2e_s = time.perf_counter() - t0
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms, world)
+    e2e_s = max_over_ranks(e2e_s, world)
+    nbytes = total * 4 + n_chunks * 16 + (st["ts"].num_streams + 1) * 8
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / (kms * 1e-3) / 1e9
+    out = {
+        "metric": "content-chunked tokens/s (Gear CDC + XXH64 fingerprints)",
+        "value": total * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u64", "data": "synthetic", "impl": "ours",
+        "config": {"workload": f"irminsul-cdc: {st['ts'].num_streams} token streams x "
+                               f"{cfg['stream_len']} ids U[0,{cfg['vocab']}), each carrying "
+                               f"segments of a {cfg['shared_segments']}-segment shared pool at "
+                               "random offsets; Gear hash over 64-token windows, threshold "
+                               f"2^{64 - cfg['log_mean']} (mean chunk {1 << cfg['log_mean']} "
+                               "tokens), XXH64 per chunk",
+                   "tokens_per_step_per_gpu": total, "chunks": n_chunks,
+                   "mean_chunk_tokens": total / max(n_chunks, 1),
+                   "parallelism": f"replicas x{world} (independent streams)",
+                   "l2": "inputs larger than L2 (%.0f MB of token ids per step)" % (total * 4 / 1e6)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": recorded_traffic("cdc_tokens"),
+                     "kernel": "cdc_flags + cdc_scan + cdc_emit + fingerprint (whole call)",
+                     "kernel_ms": kms, "algorithmic_bytes_per_step": nbytes},
+        "e2e": {"value": total * world * K / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 8 + 4},
+        "clocks": clk, "gpu_launches": launches,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle as O
+        orc = O.get()
+        sample = synth.token_streams(77, [1 << 20] * 4, vocab=cfg["vocab"], shared_segments=8)
+        t0 = time.perf_counter()
+        orc.cdc(sample.stream_off, sample.tokens, cfg["gear_seed"], st["threshold"], cfg["fp_seed"])
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": len(sample.tokens) / dt, "unit": "tokens/s", "cores": 1,
+                               "kind": "oracle",
+                               "sample": f"4 streams x 2^20 tokens of the same recipe: {dt:.1f} s"}
+    if args.check and rank == 0:
+        import oracle as O
+        out["parity_sample"] = check_cdc(st, O.get())
+    return out
+
+
 WORKLOADS = {"relocate-mla": run_relocate_mla, "splice-mla-128k": run_splice_mla_128k,
              "relocate-gqa-patch": run_relocate_gqa_patch, "splice-mla-4k": run_splice_mla_4k,
              "relocate-mla-patch": run_relocate_mla_patch, "sweep-mla": run_sweep_mla,
              "splice-mla-128k-composed": run_splice_mla_128k_composed,
              "splice-mla-128k-remap": run_splice_mla_128k_remap,
-             "window-gqa": run_window_gqa}
+             "window-gqa": run_window_gqa, "cdc-tokens": run_cdc_tokens}
 
 
 def main(argv=None):

@@ -71,7 +71,8 @@ typedef enum {
     KV_OK = 0,
     KV_ERR_INVALID_ARG = 1,  /* null pointer, bad shape, stride, alignment or directive */
     KV_ERR_OUT_OF_RANGE = 2, /* (device) a slot, block id or request index outside its pool/table */
-    KV_ERR_CAPACITY = 3,     /* kv_splice: block table row too short for seq_len + Δ */
+    KV_ERR_CAPACITY = 3,     /* kv_splice: block table row too short for seq_len + Δ;
+                                (device) kv_cdc: more chunks than max_chunks */
     KV_ERR_WORKSPACE = 4,    /* workspace NULL, misaligned or smaller than needed */
     KV_ERR_TIMEOUT = 5,      /* (device) a bounded inter-block wait ran out */
     KV_ERR_CUDA = 6,         /* a CUDA runtime call failed */
@@ -305,6 +306,56 @@ kv_status kv_relocate_noalloc(const kv_pool_desc *src, const kv_pool_desc *dst,
  * used this workspace (KV_OK, KV_ERR_OUT_OF_RANGE or KV_ERR_TIMEOUT), or
  * KV_ERR_CUDA if the synchronisation or the read failed. */
 kv_status kv_get_device_status(const void *d_workspace, kv_stream_t stream);
+
+/* ---------------------------------------------------------------------
+ * Content-defined chunking of token streams
+ * [Irminsul: MLA-native position-independent cache, §2.2, content hash
+ * keying with CDC and the fixed-window fallback S1]
+ *
+ * The registry that kv_relocate serves is keyed by content: a Gear rolling
+ * hash over windows of 64 tokens ends a chunk where it falls below a
+ * threshold, so chunk boundaries follow the tokens, not their offsets, and
+ * each chunk is named by its xxHash64 fingerprint.  The pages fix neither the
+ * Gear table nor the threshold; this library defines them as follows:
+ *   h(i) = 2*h(i-1) + G(x_i) modulo 2^64, with h = 0 before the first token of
+ *          every stream, so h(i) holds exactly the last 64 tokens;
+ *   G(x) = output number x (counting from 0) of the SplitMix64 generator seeded
+ *          with gear_seed (token ids read as unsigned 32-bit numbers);
+ *   a chunk ends after token i when h(i) < threshold (mean chunk length
+ *          2^64 / threshold tokens), and at the end of its stream;
+ *   fingerprint = XXH64 of the chunk's token ids as 4-byte little-endian
+ *          words, seeded with fp_seed.
+ * ------------------------------------------------------------------- */
+
+/* Workspace bytes kv_cdc needs for `total_tokens` tokens (256-byte aligned). */
+size_t kv_cdc_workspace_size(int64_t total_tokens);
+
+/* Chunk num_streams token streams, concatenated in d_tokens: stream s is
+ * tokens d_stream_off[s] .. d_stream_off[s+1]-1 (num_streams+1 int64 device
+ * entries, non-decreasing, first 0, last total_tokens; empty streams have no
+ * chunk).  Writes, in stream order, each chunk's exclusive end (a global
+ * token offset; a chunk starts where the previous one ends, the first at 0)
+ * to d_chunk_end[k] and its fingerprint to d_fingerprint[k], for
+ * k < max_chunks, and the number of chunks to the device scalar
+ * *d_num_chunks.  More chunks than max_chunks set the device status
+ * KV_ERR_CAPACITY (total_tokens chunks always fit); offsets that do not start
+ * at 0 or end at total_tokens set KV_ERR_OUT_OF_RANGE.  Four kernels. */
+kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total_tokens,
+                 const int32_t *d_tokens, uint64_t gear_seed, uint64_t threshold,
+                 uint64_t fp_seed, int64_t max_chunks, int64_t *d_chunk_end,
+                 uint64_t *d_fingerprint, int64_t *d_num_chunks, void *d_workspace,
+                 size_t workspace_bytes, kv_stream_t stream);
+
+/* Fingerprints of arbitrary token ranges: d_fingerprint[k] = XXH64 of tokens
+ * d_start[k] .. d_end[k]-1 (device int64 arrays, 0 <= start <= end <=
+ * total_tokens), seeded with fp_seed.  The fixed-window fallback passes
+ * consecutive windows of 128 tokens.  A range outside the tokens is skipped
+ * and sets KV_ERR_OUT_OF_RANGE in the workspace status word (only the
+ * 256-byte header of the workspace is used).  One kernel. */
+kv_status kv_fingerprint(int64_t num_ranges, const int64_t *d_start, const int64_t *d_end,
+                         int64_t total_tokens, const int32_t *d_tokens, uint64_t fp_seed,
+                         uint64_t *d_fingerprint, void *d_workspace, size_t workspace_bytes,
+                         kv_stream_t stream);
 
 /* Upper bound, in nanoseconds, of every inter-block wait inside kv_splice
  * (default 2e9).  Values <= 0 restore the default.  Process-wide. */

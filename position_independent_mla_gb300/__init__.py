@@ -112,6 +112,10 @@ def load(build_if_missing: bool = False) -> C.CDLL:
         "kv_set_kernel_events": (None, [vp, vp]),
         "kv_relocate_noalloc": (i32, [P, P, i32, i64, vp, vp, vp, vp, vp, vp, i32, i32, PP,
                                       C.POINTER(C.c_int32), vp]),
+        "kv_cdc_workspace_size": (sz, [i64]),
+        "kv_cdc": (i32, [i32, vp, i64, vp, C.c_uint64, C.c_uint64, C.c_uint64, i64, vp, vp, vp,
+                         vp, sz, vp]),
+        "kv_fingerprint": (i32, [i64, vp, vp, i64, vp, C.c_uint64, vp, vp, sz, vp]),
         "kv_status_string": (C.c_char_p, [i32]),
         "kv_version": (i32, []),
     }
@@ -318,6 +322,36 @@ def kv_patch(pool: kv_pool_desc, num_chunks: int, total_tokens: int, tok_off, ch
         C.byref(patch), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
     if check:
         _check(st, "kv_patch")
+    return st
+
+
+def kv_cdc_workspace_size(total_tokens: int) -> int:
+    return int(load().kv_cdc_workspace_size(int(total_tokens)))
+
+
+def kv_cdc(num_streams: int, stream_off, total_tokens: int, tokens, gear_seed: int,
+           threshold: int, fp_seed: int, max_chunks: int, chunk_end, fingerprint, num_chunks,
+           ws: torch.Tensor, stream=None, check: bool = True) -> int:
+    """Content-defined chunking (Irminsul §2.2); device tensors: stream_off
+    int64 [S+1], tokens int32, chunk_end int64 and fingerprint (uint64 bits in
+    an int64 tensor) [max_chunks], num_chunks int64 [1]."""
+    m = 2**64 - 1
+    st = load().kv_cdc(int(num_streams), _ptr(stream_off), int(total_tokens), _ptr(tokens),
+                       int(gear_seed) & m, int(threshold) & m, int(fp_seed) & m, int(max_chunks),
+                       _ptr(chunk_end), _ptr(fingerprint), _ptr(num_chunks), ws.data_ptr(),
+                       ws.numel() * ws.element_size(), _stream(stream))
+    if check:
+        _check(st, "kv_cdc")
+    return st
+
+
+def kv_fingerprint(num_ranges: int, start, end, total_tokens: int, tokens, fp_seed: int,
+                   fingerprint, ws: torch.Tensor, stream=None, check: bool = True) -> int:
+    st = load().kv_fingerprint(int(num_ranges), _ptr(start), _ptr(end), int(total_tokens),
+                               _ptr(tokens), int(fp_seed) & (2**64 - 1), _ptr(fingerprint),
+                               ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
+    if check:
+        _check(st, "kv_fingerprint")
     return st
 
 

@@ -817,6 +817,96 @@ kv_status kv_splice_composed_plan(const kv_pool_desc *pool, int32_t num_seqs, in
     return KV_OK;
 }
 
+size_t kv_cdc_workspace_size(int64_t total_tokens)
+{
+    if (total_tokens < 0)
+        return 0;
+    const int64_t blocks = cdc_blocks(total_tokens);
+    return kHeaderBytes + align256((size_t)blocks * kThreads * sizeof(uint32_t)) +
+           2 * align256((size_t)blocks * sizeof(int64_t));
+}
+
+kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total_tokens,
+                 const int32_t *d_tokens, uint64_t gear_seed, uint64_t threshold,
+                 uint64_t fp_seed, int64_t max_chunks, int64_t *d_chunk_end,
+                 uint64_t *d_fingerprint, int64_t *d_num_chunks, void *d_workspace,
+                 size_t workspace_bytes, kv_stream_t stream_)
+{
+    t_launches = 0;
+    if (num_streams < 0 || total_tokens < 0 || max_chunks < 0 || !d_stream_off ||
+        !d_num_chunks || (total_tokens > 0 && !d_tokens) ||
+        (max_chunks > 0 && (!d_chunk_end || !d_fingerprint)) ||
+        (num_streams == 0 && total_tokens > 0) || cdc_blocks(total_tokens) > 0x7FFFFFFF)
+        return KV_ERR_INVALID_ARG;
+    kv_status st = ws_ok(d_workspace, workspace_bytes, kv_cdc_workspace_size(total_tokens));
+    if (st != KV_OK)
+        return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    char *w = static_cast<char *>(d_workspace);
+    const int64_t blocks = cdc_blocks(total_tokens);
+    CdcParams p{};
+    p.stream_off = d_stream_off;
+    p.num_streams = num_streams;
+    p.total = total_tokens;
+    p.tokens = d_tokens;
+    p.gear_seed = gear_seed;
+    p.threshold = threshold;
+    p.fp_seed = fp_seed;
+    p.max_chunks = max_chunks;
+    p.chunk_end = d_chunk_end;
+    p.fingerprint = d_fingerprint;
+    p.num_chunks = d_num_chunks;
+    p.status = reinterpret_cast<uint32_t *>(w);
+    p.flags = reinterpret_cast<uint32_t *>(w + kHeaderBytes);
+    p.block_count = reinterpret_cast<int64_t *>(
+        w + kHeaderBytes + align256((size_t)blocks * kThreads * sizeof(uint32_t)));
+    p.block_off = p.block_count + align256((size_t)blocks * sizeof(int64_t)) / sizeof(int64_t);
+    p.blocks = (int32_t)blocks;
+    KV_CUDA(cudaMemsetAsync(w, 0, kHeaderBytes, stream));
+    if (blocks == 0) {
+        KV_CUDA(cudaMemsetAsync(d_num_chunks, 0, sizeof(int64_t), stream));
+        return KV_OK;
+    }
+    KV_CUDA(mark(t_ev_start, stream));
+    KV_CUDA(launch_cdc(p, stream));
+    KV_CUDA(mark(t_ev_stop, stream));
+    t_launches = kCdcLaunches - (std::min(max_chunks, total_tokens) > 0 ? 0 : 1);
+    return KV_OK;
+}
+
+kv_status kv_fingerprint(int64_t num_ranges, const int64_t *d_start, const int64_t *d_end,
+                         int64_t total_tokens, const int32_t *d_tokens, uint64_t fp_seed,
+                         uint64_t *d_fingerprint, void *d_workspace, size_t workspace_bytes,
+                         kv_stream_t stream_)
+{
+    t_launches = 0;
+    if (num_ranges < 0 || total_tokens < 0 ||
+        (num_ranges > 0 && (!d_start || !d_end || !d_fingerprint || (total_tokens > 0 && !d_tokens))))
+        return KV_ERR_INVALID_ARG;
+    kv_status st = ws_ok(d_workspace, workspace_bytes, kHeaderBytes);
+    if (st != KV_OK)
+        return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    KV_CUDA(cudaMemsetAsync(d_workspace, 0, kHeaderBytes, stream));
+    if (num_ranges == 0)
+        return KV_OK;
+    FingerprintParams f{};
+    f.tokens = d_tokens;
+    f.total = total_tokens;
+    f.start = d_start;
+    f.end = d_end;
+    f.count = nullptr;
+    f.cap = num_ranges;
+    f.seed = fp_seed;
+    f.fingerprint = d_fingerprint;
+    f.status = static_cast<uint32_t *>(d_workspace);
+    KV_CUDA(mark(t_ev_start, stream));
+    KV_CUDA(launch_fingerprint(f, stream));
+    KV_CUDA(mark(t_ev_stop, stream));
+    t_launches = 1;
+    return KV_OK;
+}
+
 kv_status kv_get_device_status(const void *d_workspace, kv_stream_t stream)
 {
     if (!d_workspace)

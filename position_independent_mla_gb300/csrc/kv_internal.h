@@ -17,7 +17,7 @@ constexpr int kTileGqa4 = 32;         // rows per tile for 4 x 128 GQA rows
 constexpr int kTileMha = 4;           // rows per tile for 32 x 128 MHA rows
 
 // Device status codes (same values as kv_status).
-enum : uint32_t { kStatusOk = 0, kStatusOutOfRange = 2, kStatusTimeout = 5 };
+enum : uint32_t { kStatusOk = 0, kStatusOutOfRange = 2, kStatusCapacity = 3, kStatusTimeout = 5 };
 
 // A pool as the kernels see it: byte addresses and byte strides.
 struct PoolView {
@@ -158,6 +158,37 @@ struct TableParams {
     int32_t head_dim; // d
     double base;
     float4 *table;
+};
+
+// Content-defined chunking of token streams (kv_cdc).
+struct CdcParams {
+    const int64_t *stream_off; // [num_streams + 1]
+    int32_t num_streams;
+    int64_t total;             // tokens
+    const int32_t *tokens;
+    uint64_t gear_seed, threshold, fp_seed;
+    int64_t max_chunks;
+    int64_t *chunk_end;        // [max_chunks]
+    uint64_t *fingerprint;     // [max_chunks]
+    int64_t *num_chunks;       // device scalar
+    uint32_t *status;
+    uint32_t *flags;           // workspace: one word per 32 positions
+    int64_t *block_count;      // workspace: per block
+    int64_t *block_off;        // workspace: per block
+    int32_t blocks;
+};
+
+// Fingerprints of token ranges (kv_fingerprint, and the last step of kv_cdc).
+struct FingerprintParams {
+    const int32_t *tokens;
+    int64_t total;
+    const int64_t *start; // nullptr: consecutive ranges, start = previous end
+    const int64_t *end;
+    const int64_t *count; // nullptr: cap ranges; else min(*count, cap)
+    int64_t cap;
+    uint64_t seed;
+    uint64_t *fingerprint;
+    uint32_t *status;
 };
 
 } // namespace kvr

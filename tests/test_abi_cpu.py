@@ -117,3 +117,24 @@ def test_workspace_checks(lib):
                                      None) == kv.KV_ERR_WORKSPACE
     # too small
     assert lib.kv_check_wait_timeout(C.c_void_p(1 << 24), 64, 1000, None) == kv.KV_ERR_WORKSPACE
+
+
+def test_cdc_host_checks(lib):
+    ws = torch.empty(1 << 12, dtype=torch.uint8)
+    assert kv.kv_cdc_workspace_size(-1) == 0
+    assert kv.kv_cdc_workspace_size(0) == 256
+    assert kv.kv_cdc_workspace_size(1 << 20) > kv.kv_cdc_workspace_size(1 << 10) > 256
+    # negative stream count, missing offsets, tokens without streams
+    assert kv.kv_cdc(-1, None, 0, None, 0, 0, 0, 0, None, None, None, ws,
+                     check=False) == kv.KV_ERR_INVALID_ARG
+    assert kv.kv_cdc(1, None, 10, C.c_void_p(256), 0, 0, 0, 10, C.c_void_p(256),
+                     C.c_void_p(256), C.c_void_p(256), ws, check=False) == kv.KV_ERR_INVALID_ARG
+    assert kv.kv_cdc(0, C.c_void_p(256), 10, C.c_void_p(256), 0, 0, 0, 10, C.c_void_p(256),
+                     C.c_void_p(256), C.c_void_p(256), ws, check=False) == kv.KV_ERR_INVALID_ARG
+    # workspace too small for the token count
+    small = C.c_void_p(1 << 24)
+    assert lib.kv_cdc(1, C.c_void_p(256), 1 << 20, C.c_void_p(256), 0, 0, 0, 10,
+                      C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), small, 256,
+                      None) == kv.KV_ERR_WORKSPACE
+    assert kv.kv_fingerprint(3, None, None, 10, None, 0, None, ws,
+                             check=False) == kv.KV_ERR_INVALID_ARG

@@ -339,7 +339,7 @@ size_t kv_cdc_workspace_size(int64_t total_tokens);
  * k < max_chunks, and the number of chunks to the device scalar
  * *d_num_chunks.  More chunks than max_chunks set the device status
  * KV_ERR_CAPACITY (total_tokens chunks always fit); offsets that do not start
- * at 0 or end at total_tokens set KV_ERR_OUT_OF_RANGE.  Four kernels. */
+ * at 0 or end at total_tokens set KV_ERR_OUT_OF_RANGE.  Three kernels. */
 kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total_tokens,
                  const int32_t *d_tokens, uint64_t gear_seed, uint64_t threshold,
                  uint64_t fp_seed, int64_t max_chunks, int64_t *d_chunk_end,

@@ -823,7 +823,7 @@ size_t kv_cdc_workspace_size(int64_t total_tokens)
         return 0;
     const int64_t blocks = cdc_blocks(total_tokens);
     return kHeaderBytes + align256((size_t)blocks * kThreads * sizeof(uint32_t)) +
-           2 * align256((size_t)blocks * sizeof(int64_t));
+           4 * align256((size_t)blocks * sizeof(int64_t));
 }
 
 kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total_tokens,
@@ -860,7 +860,10 @@ kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total
     p.flags = reinterpret_cast<uint32_t *>(w + kHeaderBytes);
     p.block_count = reinterpret_cast<int64_t *>(
         w + kHeaderBytes + align256((size_t)blocks * kThreads * sizeof(uint32_t)));
-    p.block_off = p.block_count + align256((size_t)blocks * sizeof(int64_t)) / sizeof(int64_t);
+    const size_t per = align256((size_t)blocks * sizeof(int64_t)) / sizeof(int64_t);
+    p.block_last = p.block_count + per;
+    p.block_off = p.block_last + per;
+    p.block_prev_end = p.block_off + per;
     p.blocks = (int32_t)blocks;
     KV_CUDA(cudaMemsetAsync(w, 0, kHeaderBytes, stream));
     if (blocks == 0) {
@@ -870,7 +873,7 @@ kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total
     KV_CUDA(mark(t_ev_start, stream));
     KV_CUDA(launch_cdc(p, stream));
     KV_CUDA(mark(t_ev_stop, stream));
-    t_launches = kCdcLaunches - (std::min(max_chunks, total_tokens) > 0 ? 0 : 1);
+    t_launches = kCdcLaunches;
     return KV_OK;
 }
 
@@ -895,8 +898,7 @@ kv_status kv_fingerprint(int64_t num_ranges, const int64_t *d_start, const int64
     f.total = total_tokens;
     f.start = d_start;
     f.end = d_end;
-    f.count = nullptr;
-    f.cap = num_ranges;
+    f.count = num_ranges;
     f.seed = fp_seed;
     f.fingerprint = d_fingerprint;
     f.status = static_cast<uint32_t *>(d_workspace);

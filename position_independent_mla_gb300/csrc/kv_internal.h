@@ -173,19 +173,20 @@ struct CdcParams {
     int64_t *num_chunks;       // device scalar
     uint32_t *status;
     uint32_t *flags;           // workspace: one word per 32 positions
-    int64_t *block_count;      // workspace: per block
-    int64_t *block_off;        // workspace: per block
+    int64_t *block_count;      // workspace: chunk ends per block
+    int64_t *block_last;       // workspace: last chunk end in the block, or -1
+    int64_t *block_off;        // workspace: chunks before the block
+    int64_t *block_prev_end;   // workspace: last chunk end before the block, or 0
     int32_t blocks;
 };
 
-// Fingerprints of token ranges (kv_fingerprint, and the last step of kv_cdc).
+// Fingerprints of token ranges (kv_fingerprint).
 struct FingerprintParams {
     const int32_t *tokens;
     int64_t total;
-    const int64_t *start; // nullptr: consecutive ranges, start = previous end
+    const int64_t *start;
     const int64_t *end;
-    const int64_t *count; // nullptr: cap ranges; else min(*count, cap)
-    int64_t cap;
+    int64_t count;
     uint64_t seed;
     uint64_t *fingerprint;
     uint32_t *status;

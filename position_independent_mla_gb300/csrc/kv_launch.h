@@ -30,11 +30,11 @@ cudaError_t launch_remap(const RemapParams &p, RowKind kind, cudaStream_t stream
 constexpr int32_t kMaxRemapBlocks = 48 * 1024; // block-table entries one commit block holds
 cudaError_t launch_wait_check(uint32_t *flag, uint32_t *status, int64_t limit_ns,
                               cudaStream_t stream);
-// Content-defined chunking: flags, scan, emit and fingerprint kernels.
+// Content-defined chunking: flags, scan, emit (+ fingerprint) kernels.
 int64_t cdc_blocks(int64_t total_tokens);
 cudaError_t launch_cdc(const CdcParams &p, cudaStream_t stream);
 cudaError_t launch_fingerprint(const FingerprintParams &p, cudaStream_t stream);
-constexpr int kCdcLaunches = 4;
+constexpr int kCdcLaunches = 3;
 
 // Rows per tile of each kind (splice workspace sizing).
 inline int tile_rows(RowKind kind)

@@ -61,16 +61,20 @@ def hbm_peak():
 
 # Sources that build each workload's dominant kernel (its own translation
 # unit, the shared device headers and the launch dispatch).
-_COMMON_SOURCES = ("kv_device.cuh", "kv_tiles.cuh", "kv_internal.h", "kv_launch.h", "kv_api.cu")
+# Sources that decide a workload's row-moving kernels (their device code and
+# launch parameters): a recorded DRAM traffic figure is used only while these
+# files are unchanged.  kv_api.cu is included where it plans the launch (splice
+# tiles, remapping); it only forwards arguments for relocation and chunking.
+_DEVICE_SOURCES = ("kv_device.cuh", "kv_tiles.cuh", "kv_internal.h")
 KERNEL_SOURCES = {
-    "relocate_mla": ("kv_relocate.cu",) + _COMMON_SOURCES,
-    "splice_mla_128k": ("kv_splice.cu",) + _COMMON_SOURCES,
-    "relocate_gqa_patch": ("kv_patch_tc.cu",) + _COMMON_SOURCES,
-    "relocate_mla_patch": ("kv_patch_tc.cu",) + _COMMON_SOURCES,
-    "splice_mla_128k_composed": ("kv_splice.cu",) + _COMMON_SOURCES,
-    "splice_mla_128k_remap": ("kv_splice.cu",) + _COMMON_SOURCES,
-    "window_gqa": ("kv_splice.cu", "kv_patch_tc.cu") + _COMMON_SOURCES,
-    "cdc_tokens": ("kv_cdc.cu",) + _COMMON_SOURCES,
+    "relocate_mla": ("kv_relocate.cu",) + _DEVICE_SOURCES,
+    "splice_mla_128k": ("kv_splice.cu", "kv_api.cu") + _DEVICE_SOURCES,
+    "relocate_gqa_patch": ("kv_patch_tc.cu",) + _DEVICE_SOURCES,
+    "relocate_mla_patch": ("kv_patch_tc.cu",) + _DEVICE_SOURCES,
+    "splice_mla_128k_composed": ("kv_splice.cu", "kv_api.cu") + _DEVICE_SOURCES,
+    "splice_mla_128k_remap": ("kv_splice.cu", "kv_api.cu") + _DEVICE_SOURCES,
+    "window_gqa": ("kv_splice.cu", "kv_patch_tc.cu", "kv_api.cu") + _DEVICE_SOURCES,
+    "cdc_tokens": ("kv_cdc.cu", "kv_device.cuh", "kv_internal.h"),
 }
 
 
@@ -1796,6 +1800,141 @@ def run_sweep_mla(args, rank, world, local):
 
 
 # ---------------------------------------------------------------------------
+# Workload: the other row families (GQA 4 x 128, MHA 32 x 128) and
+# interleaved RoPE pairs (MLA), relocation without a patch
+# ---------------------------------------------------------------------------
+
+FAMILIES = [
+    # name, layers, copy_dim, rot heads, head dim, rope base, pairs, requests, chunks/req, chunk len
+    dict(name="gqa4-qwen2.5-7b", layers=28, copy_dim=512, heads=4, hd=128, base=1000000.0,
+         il=0, num_reqs=16, chunks_per_req=64, chunk_len=576, n_pool_chunks=256),
+    dict(name="mha-llama2-7b", layers=32, copy_dim=4096, heads=32, hd=128, base=10000.0,
+         il=0, num_reqs=8, chunks_per_req=32, chunk_len=512, n_pool_chunks=128),
+    dict(name="mla-interleaved", layers=61, copy_dim=512, heads=1, hd=64, base=10000.0,
+         il=1, num_reqs=32, chunks_per_req=16, chunk_len=1152, n_pool_chunks=256),
+]
+
+
+def check_family_sample(fam, wl, src_c, src_r, dst_c, dst_r, orc, n_rows=200, seed=19) -> dict:
+    """Sampled parity: random (token, layer) rows of the relocation; copy part
+    against the source row, every rotary head against the oracle's rotation."""
+    rng = np.random.default_rng(seed)
+    toks = rng.integers(0, wl.total_tokens, n_rows)
+    lays = rng.integers(0, fam["layers"], n_rows)
+    chunk = np.searchsorted(wl.tok_off, toks, side="right") - 1
+    pos = wl.chunk_dst_pos[chunk] + (toks - wl.tok_off[chunk])
+    dslot = wl.block_tables[wl.chunk_req[chunk], pos // 64].astype(np.int64) * 64 + pos % 64
+    sslot = wl.src_slots[toks].astype(np.int64)
+    li = torch.from_numpy(lays).cuda()
+    s_c = synth.bits(src_c[li, torch.from_numpy(sslot).cuda()].cpu())
+    d_c = synth.bits(dst_c[li, torch.from_numpy(dslot).cuda()].cpu())
+    s_r = synth.bits(src_r[li, torch.from_numpy(sslot).cuda()].cpu())
+    d_r = synth.bits(dst_r[li, torch.from_numpy(dslot).cuda()].cpu())
+    hd = fam["hd"]
+    want = np.stack([np.concatenate([orc.rotate_bf16(s_r[i, h * hd:(h + 1) * hd],
+                                                     int(wl.delta[chunk[i]]), fam["base"],
+                                                     interleaved=bool(fam["il"]))
+                                     for h in range(fam["heads"])]) for i in range(n_rows)])
+    r = ulp_stats(d_r, want)
+    return {"rows": n_rows, "copy_rows_differing": int((s_c != d_c).any(axis=1).sum()),
+            "rot_exact": r["exact"], "rot_one_ulp": r["one_ulp"], "rot_beyond": r["beyond"]}
+
+
+def run_families(args, rank, world, local):
+    """Relocation (no patch) for the row families beside the headline MLA: GQA with
+    4 KV heads (Qwen2.5-7B shape), MHA with 32 heads (Llama-2-7B shape), and MLA
+    rows whose k_pe pairs are interleaved -- one line, one entry per family."""
+    import position_independent_mla_gb300 as kv
+
+    K, W = args.steps, args.warmup
+    peak, peak_kind = hbm_peak()
+    clocks = ClockSampler(local)
+    clocks.start()
+    res, tot_tok, tot_ms, launches, main = [], 0, 0.0, 0, None
+    orc = None
+    if args.check and rank == 0:
+        import oracle as O
+        orc = O.get()
+    for fam in FAMILIES:
+        f = dict(fam)
+        if args.small:
+            f.update(num_reqs=1, n_pool_chunks=16)
+        wl = synth.relocate_workload(6006 + 100 * rank, num_reqs=f["num_reqs"],
+                                     chunks_per_req=f["chunks_per_req"], len_lo=f["chunk_len"],
+                                     len_hi=f["chunk_len"], delta_lo=-32768, delta_hi=32768,
+                                     n_pool_chunks=f["n_pool_chunks"], base_hi=32768)
+        L, rw = f["layers"], f["heads"] * f["hd"]
+        src_c = torch.empty((L, wl.src_slots_total, f["copy_dim"]), dtype=torch.bfloat16,
+                            device="cuda")
+        src_r = torch.empty((L, wl.src_slots_total, rw), dtype=torch.bfloat16, device="cuda")
+        fill_normal_(src_c, 6007)
+        fill_normal_(src_r, 6008)
+        dst_c = torch.zeros((L, wl.dst_slots_total, f["copy_dim"]), dtype=torch.bfloat16,
+                            device="cuda")
+        dst_r = torch.zeros((L, wl.dst_slots_total, rw), dtype=torch.bfloat16, device="cuda")
+        sd = kv.pool_desc(src_c, src_r, 64, f["heads"], f["base"], pair_convention=f["il"])
+        dd = kv.pool_desc(dst_c, dst_r, 64, f["heads"], f["base"], pair_convention=f["il"])
+        dev = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).cuda()
+               for k in ("tok_off", "src_slots", "chunk_req", "chunk_dst_pos", "delta",
+                         "block_tables")}
+        ws = kv.workspace(dd, wl.total_tokens, wl.num_chunks)
+
+        def call():
+            kv.kv_relocate(sd, dd, wl.num_chunks, wl.total_tokens, dev["tok_off"],
+                           dev["src_slots"], dev["chunk_req"], dev["chunk_dst_pos"],
+                           dev["delta"], dev["block_tables"], wl.block_tables.shape[0],
+                           wl.block_tables.shape[1], None, ws)
+            return kv.kv_last_launch_count()
+
+        barrier(world)
+        ms, kms, n_l = _timed(call, K, W)
+        assert kv.kv_get_device_status(ws) == kv.KV_OK
+        launches += n_l
+        nbytes = wl.total_tokens * (L * 2 * 2 * (f["copy_dim"] + rw) + 4)
+        entry = {"family": f["name"], "layers": L, "row_bf16": f["copy_dim"] + rw,
+                 "pairs": "interleaved" if f["il"] else "rotate-half",
+                 "tokens": wl.total_tokens, "kernel_ms": kms,
+                 "achieved_gbs": nbytes / (kms * 1e-3) / 1e9,
+                 "frac": nbytes / (kms * 1e-3) / 1e9 / peak, "algorithmic_bytes": nbytes}
+        if orc is not None:
+            entry["parity_sample"] = check_family_sample(f, wl, src_c, src_r, dst_c, dst_r, orc)
+        res.append(entry)
+        tot_tok += wl.total_tokens * world
+        tot_ms += max_over_ranks(ms, world)
+        if main is None or nbytes > main["algorithmic_bytes"]:
+            main = entry
+        del src_c, src_r, dst_c, dst_r, ws, dev
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    clk = clocks.stop()
+    out = {
+        "metric": "relocated KV tokens/s (all layers)",
+        "value": tot_tok / (tot_ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": tot_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "impl": "ours",
+        "config": {"workload": "families: relocation without a patch for "
+                               + ", ".join(e["family"] for e in res)
+                               + " (one step = one relocation of each)",
+                   "families": res, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (%.0f GB moved per step)"
+                         % (sum(e["algorithmic_bytes"] for e in res) / 1e9)},
+        "roofline": {"bound": "hbm", "achieved": main["achieved_gbs"], "peak": peak,
+                     "unit": "GB/s", "frac": main["frac"], "peak_kind": peak_kind,
+                     "traffic": None, "kernel": f"relocate_kernel ({main['family']})",
+                     "kernel_ms": main["kernel_ms"],
+                     "algorithmic_bytes_per_launch": main["algorithmic_bytes"]},
+        "e2e": None, "clocks": clk, "gpu_launches": launches,
+    }
+    if orc is not None:
+        agg = {}
+        for e in res:
+            for k2, v2 in e["parity_sample"].items():
+                agg[k2] = agg.get(k2, 0) + v2
+        out["parity_sample"] = agg
+    return out
+
+
+# ---------------------------------------------------------------------------
 # Workload: Irminsul content-defined chunking of token streams
 # ---------------------------------------------------------------------------
 
@@ -1929,7 +2068,8 @@ WORKLOADS = {"relocate-mla": run_relocate_mla, "splice-mla-128k": run_splice_mla
              "relocate-mla-patch": run_relocate_mla_patch, "sweep-mla": run_sweep_mla,
              "splice-mla-128k-composed": run_splice_mla_128k_composed,
              "splice-mla-128k-remap": run_splice_mla_128k_remap,
-             "window-gqa": run_window_gqa, "cdc-tokens": run_cdc_tokens}
+             "window-gqa": run_window_gqa, "cdc-tokens": run_cdc_tokens,
+             "families": run_families}
 
 
 def main(argv=None):

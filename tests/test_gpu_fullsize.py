@@ -36,7 +36,8 @@ def _assert_clean(sample: dict, what: str):
 
 @pytest.mark.parametrize("workload", ["relocate-mla", "splice-mla-128k", "relocate-gqa-patch",
                                       "relocate-mla-patch", "splice-mla-128k-composed",
-                                      "splice-mla-128k-remap", "window-gqa", "cdc-tokens"])
+                                      "splice-mla-128k-remap", "window-gqa", "cdc-tokens",
+                                      "families"])
 def test_full_size_sampled_parity(workload):
     out = _run(workload)
     _assert_clean(out["parity_sample"], workload)

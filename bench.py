@@ -75,6 +75,7 @@ KERNEL_SOURCES = {
     "splice_mla_128k_remap": ("kv_splice.cu", "kv_api.cu") + _DEVICE_SOURCES,
     "window_gqa": ("kv_splice.cu", "kv_patch_tc.cu", "kv_api.cu") + _DEVICE_SOURCES,
     "cdc_tokens": ("kv_cdc.cu", "kv_device.cuh", "kv_internal.h"),
+    "families": ("kv_relocate.cu",) + _DEVICE_SOURCES,
 }
 
 
@@ -1920,7 +1921,8 @@ def run_families(args, rank, world, local):
                          % (sum(e["algorithmic_bytes"] for e in res) / 1e9)},
         "roofline": {"bound": "hbm", "achieved": main["achieved_gbs"], "peak": peak,
                      "unit": "GB/s", "frac": main["frac"], "peak_kind": peak_kind,
-                     "traffic": None, "kernel": f"relocate_kernel ({main['family']})",
+                     "traffic": recorded_traffic("families"),
+                     "kernel": f"relocate_kernel ({main['family']})",
                      "kernel_ms": main["kernel_ms"],
                      "algorithmic_bytes_per_launch": main["algorithmic_bytes"]},
         "e2e": None, "clocks": clk, "gpu_launches": launches,

@@ -164,9 +164,9 @@ __device__ __forceinline__ void stage_starts(const CdcParams &p, int64_t base, i
         if (tid == 0)
             *s_found = b;
         __syncthreads();
-        const int idx = a + tid * step;
+        const int64_t idx = (int64_t)a + (int64_t)tid * step;
         if (idx <= b && p.stream_off[idx] >= lo)
-            atomicMin(s_found, idx);
+            atomicMin(s_found, (int)idx);
         __syncthreads();
         const int f = *s_found;
         __syncthreads();

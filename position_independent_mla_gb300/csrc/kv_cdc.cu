@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(kThreadsCdc) cdc_emit_kernel(const __grid_cons
     __shared__ int64_t s_wsum[kThreadsCdc / 32];
     __shared__ int64_t s_wmax[kThreadsCdc / 32];
     __shared__ int64_t s_la[kMaxLong], s_lb[kMaxLong], s_lk[kMaxLong];
+    __shared__ int16_t s_order[kMaxLong]; // long chunks, longest first
     __shared__ int s_nlong;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t tile0 = (int64_t)blockIdx.x * kTileCdc;
@@ -456,13 +457,26 @@ __global__ void __launch_bounds__(kThreadsCdc) cdc_emit_kernel(const __grid_cons
     }
     __syncthreads();
 
-    // long chunks: quad q = tid / 4 takes entries q, q + 64, ...
+    // long chunks, longest first, so that the quads of a warp (which wait for
+    // one another) get chunks of similar length; quad q takes the q-th, the
+    // (q + 64)-th, ... of them
     const int nlong = min(s_nlong, kMaxLong);
+    if (tid < nlong) {
+        const int64_t len = s_lb[tid] - s_la[tid];
+        int rank = 0;
+        for (int j = 0; j < nlong; ++j) {
+            const int64_t lj = s_lb[j] - s_la[j];
+            rank += (lj > len) || (lj == len && j < tid);
+        }
+        s_order[rank] = (int16_t)tid;
+    }
+    __syncthreads();
     const int quad = tid >> 2, a = tid & 3;
     const int rounds = (nlong + kThreadsCdc / 4 - 1) / (kThreadsCdc / 4);
     for (int r = 0; r < rounds; ++r) {
-        const int i = quad + r * (kThreadsCdc / 4);
-        const bool mine = i < nlong;
+        const int ri = quad + r * (kThreadsCdc / 4);
+        const bool mine = ri < nlong;
+        const int i = mine ? s_order[ri] : 0;
         const int64_t ca = mine ? s_la[i] : 0, cb = mine ? s_lb[i] : 0;
         const uint64_t seed = p.fp_seed;
         uint64_t v = a == 0 ? seed + kP1 + kP2 : a == 1 ? seed + kP2 : a == 2 ? seed : seed - kP1;

@@ -215,7 +215,9 @@ struct TcSmem {
 // memory while the block forms the A operand and the MMAs run; then every
 // thread rewrites its (row, column group) of the tile in shared memory and
 // threads 0..127 write the rows back with bulk copies.
-template <class G, bool RELOC>
+// PF: fetch the next tile's U rows while this tile is rewritten (the GQA
+// relocation's block has no registers to spare for them).
+template <class G, bool RELOC, bool PF = true>
 __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaunch &tl,
                                               const int bx)
 {
@@ -339,6 +341,26 @@ __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaun
     if (owner && ntiles > 0)
         row_slots(0, src, dst);
     uint32_t ph_x = 0, ph_mma = 0;
+    // U rows of a tile for the A operand, one or two (row, 8 ranks) items per thread
+    constexpr int kUItems = (G::ROWS * 2 + G::NT - 1) / G::NT;
+    float u_next[kUItems][8];
+    auto load_u = [&](int64_t t) {
+#pragma unroll
+        for (int it = 0; it < kUItems; ++it) {
+            const int e = tid + it * G::NT;
+            const int r = e >> 1, k0 = (e & 1) * 8;
+            const int64_t i = t * G::ROWS + r;
+            if (e < G::ROWS * 2 && i < n) {
+                load_factor8(p.patch.u[ch] + (int64_t)l * p.patch.u_ls[ch] +
+                                 (u0 + i) * p.patch.u_ts[ch],
+                             k0, m, u_next[it]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    u_next[it][q] = 0.0f;
+            }
+        }
+    };
     for (int64_t t = 0; t < ntiles; ++t) {
         int64_t my_dst = -1;
         if (owner) {
@@ -355,23 +377,20 @@ __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaun
                 row_slots(t + 1, src, dst);
         }
         if (patched) {
-            // A operand: the tile's U rows split into bf16 hi / lo (zero past the chunk)
-            for (int e = tid; e < G::ROWS * 2; e += G::NT) {
-                const int r = e >> 1, k0 = (e & 1) * 8;
-                const int64_t i = t * G::ROWS + r;
-                unsigned char *a_hi = smem + S::A_OFF + (r / M) * 2 * A_BYTES;
-                unsigned char *a_lo = a_hi + A_BYTES;
-                float u[8];
-                if (i < n) {
-                    load_factor8(p.patch.u[ch] + (int64_t)l * p.patch.u_ls[ch] +
-                                     (u0 + i) * p.patch.u_ts[ch],
-                                 k0, m, u);
-                } else {
+            // A operand: the tile's U rows (fetched during the previous tile's
+            // rewrite) split into bf16 hi / lo (zero past the chunk)
+            if (t == 0 || !PF)
+                load_u(t);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        u[q] = 0.0f;
+            for (int it = 0; it < kUItems; ++it) {
+                const int e = tid + it * G::NT;
+                if (e < G::ROWS * 2) {
+                    const int r = e >> 1, k0 = (e & 1) * 8;
+                    unsigned char *a_hi = smem + S::A_OFF + (r / M) * 2 * A_BYTES;
+                    unsigned char *a_lo = a_hi + A_BYTES;
+                    split_store8(u_next[it], a_hi + kmajor_off(r % M, k0),
+                                 a_lo + kmajor_off(r % M, k0));
                 }
-                split_store8(u, a_hi + kmajor_off(r % M, k0), a_lo + kmajor_off(r % M, k0));
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             fence_before();
@@ -407,6 +426,8 @@ __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaun
         fence_after();
         if (!s_ok)
             break;
+        if (PF && patched && t + 1 < ntiles)
+            load_u(t + 1); // lands while this tile is rewritten
 
         // rewrite my (row, column group) of the tile in place
         if (patched && rotate) {
@@ -531,7 +552,7 @@ template <class G, bool RELOC>
 __global__ void __launch_bounds__(G::NT, G::MIN_BLOCKS)
 patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
 {
-    patch_tc_body<G, RELOC>(p, tl, (int)blockIdx.x);
+    patch_tc_body<G, RELOC, !(RELOC && G::NB == 256)>(p, tl, (int)blockIdx.x);
 }
 
 // MLA rows in one launch: the first n_kv blocks take the latent c_KV in

@@ -134,9 +134,13 @@ def test_relocate_with_fused_patch_large_rank(orc, m):
     check_pool(dst, f"relocate+patch rank {m}", copy_exact=False)
 
 
+# chunks of 1-150 tokens (mostly under one 128-row tile) and of 200-600
+# tokens (several tiles per block); in place, MLA's c_KV and k_pe slices are
+# launched separately
 @pytest.mark.parametrize("shape", ["mla", "gqa"])
-def test_standalone_patch(orc, shape):
-    wl, src, dst, dev = _reloc_case(shape, 240)
+@pytest.mark.parametrize("lens", [(1, 150), (200, 600)])
+def test_standalone_patch(orc, shape, lens):
+    wl, src, dst, dev = _reloc_case(shape, 240, lo=lens[0], hi=lens[1])
     m = 4 if shape == "mla" else 12
     us = [synth.f32_normal((L, wl.total_tokens, m), 241 + i, std=0.05) for i in range(2)]
     widths = (512, 64) if shape == "mla" else (1024, 1024)
@@ -148,7 +152,6 @@ def test_standalone_patch(orc, shape):
                 dev["chunk_dst_pos"], dev["block_tables"], wl.block_tables.shape[0],
                 wl.block_tables.shape[1], pd, ws)
     assert kv.kv_get_device_status(ws) == kv.KV_OK
-    # in place, MLA's c_KV and k_pe slices are launched separately
     assert kv.kv_last_launch_count() == (2 if shape == "mla" else 1)
     assert orc.patch_apply(dst.orc, wl.tok_off, wl.chunk_req, wl.chunk_dst_pos, wl.block_tables,
                            O.Patch(m, [x.numpy() for x in us],

@@ -65,3 +65,21 @@ def test_oracle_on_every_core_counts_every_unit():
     finally:
         cores.close()
     assert ntok == 32 and dt > 0
+
+
+def test_reference_arm_prints_one_complete_line(capsys):
+    """bench.py --impl reference: the oracle on every host core, one JSON line
+    with the contract's keys (no GPU needed)."""
+    import json
+
+    import bench
+
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    line = capsys.readouterr().out.strip().splitlines()[-1]
+    d = json.loads(line)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "dtype", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0

@@ -429,8 +429,11 @@ __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaun
         if (PF && patched && t + 1 < ntiles)
             load_u(t + 1); // lands while this tile is rewritten
 
-        // rewrite my (row, column group) of the tile in place
-        if (patched && rotate) {
+        // rewrite my (row, column group) of the tile in place; a warp whose 32
+        // rows all lie past the chunk's end has nothing to rewrite
+        const bool warp_rows = t * G::ROWS + rt * M + (warp & 3) * 32 < n;
+        if (!warp_rows) {
+        } else if (patched && rotate) {
             const ulonglong2 *cc = reinterpret_cast<const ulonglong2 *>(cs_c);
             const ulonglong2 *ss = reinterpret_cast<const ulonglong2 *>(cs_s);
 #pragma unroll

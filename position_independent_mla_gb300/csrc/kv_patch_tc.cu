@@ -215,9 +215,7 @@ struct TcSmem {
 // memory while the block forms the A operand and the MMAs run; then every
 // thread rewrites its (row, column group) of the tile in shared memory and
 // threads 0..127 write the rows back with bulk copies.
-// PF: fetch the next tile's U rows while this tile is rewritten (the GQA
-// relocation's block has no registers to spare for them).
-template <class G, bool RELOC, bool PF = true>
+template <class G, bool RELOC>
 __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaunch &tl,
                                               const int bx)
 {
@@ -379,7 +377,7 @@ __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaun
         if (patched) {
             // A operand: the tile's U rows (fetched during the previous tile's
             // rewrite) split into bf16 hi / lo (zero past the chunk)
-            if (t == 0 || !PF)
+            if (t == 0)
                 load_u(t);
 #pragma unroll
             for (int it = 0; it < kUItems; ++it) {
@@ -426,7 +424,7 @@ __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaun
         fence_after();
         if (!s_ok)
             break;
-        if (PF && patched && t + 1 < ntiles)
+        if (patched && t + 1 < ntiles)
             load_u(t + 1); // lands while this tile is rewritten
 
         // rewrite my (row, column group) of the tile in place; a warp whose 32
@@ -436,7 +434,9 @@ __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaun
         } else if (patched && rotate) {
             const ulonglong2 *cc = reinterpret_cast<const ulonglong2 *>(cs_c);
             const ulonglong2 *ss = reinterpret_cast<const ulonglong2 *>(cs_s);
-#pragma unroll
+            // one 16-frequency group at a time: the registers this leaves free
+            // hold the next tile's U rows
+#pragma unroll 1
             for (int f0 = 0; f0 < G::HALF; f0 += 16) {
                 uint32_t a1[16], a2[16];
                 tmem_ld16(t_row + (uint32_t)f0, a1);
@@ -555,7 +555,7 @@ template <class G, bool RELOC>
 __global__ void __launch_bounds__(G::NT, G::MIN_BLOCKS)
 patch_tc_kernel(const __grid_constant__ RelocParams p, const TcLaunch tl)
 {
-    patch_tc_body<G, RELOC, !(RELOC && G::NB == 256)>(p, tl, (int)blockIdx.x);
+    patch_tc_body<G, RELOC>(p, tl, (int)blockIdx.x);
 }
 
 // MLA rows in one launch: the first n_kv blocks take the latent c_KV in

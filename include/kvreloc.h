@@ -52,7 +52,9 @@
  *  - Alignment: copy_base, rot_base and every stride must give 16-byte aligned
  *    rows (strides multiples of 8 elements); copy_dim % 8 == 0;
  *    rot_head_dim % 16 == 0.  Patch factors: 16-byte aligned, strides
- *    multiples of 4 floats, rank a multiple of 4.
+ *    multiples of 4 floats, rank a multiple of 4.  Index arrays are naturally
+ *    aligned (4 bytes for int32, 8 for int64); a misaligned one is rejected
+ *    with KV_ERR_INVALID_ARG.
  */
 #ifndef KVRELOC_H
 #define KVRELOC_H

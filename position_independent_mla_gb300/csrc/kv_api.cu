@@ -32,6 +32,10 @@ constexpr size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Natural alignment of a device array of n-byte elements (NULL passes: the
+// callers check presence separately).
+bool aligned_to(const void *p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) & (n - 1)) == 0; }
+
 // Shape and layout checks shared by every call.
 bool pool_ok(const kv_pool_desc *p)
 {
@@ -108,6 +112,8 @@ kv_status patch_view(const kv_patch_desc *d, PatchView *pv, bool *any)
     if (d->rank < 4 || d->rank > kMaxRank || d->rank % 4 != 0)
         return KV_ERR_INVALID_ARG;
     pv->m = d->rank;
+    if (!aligned_to(d->d_u_chunk_tok, 8) || !aligned_to(d->d_v_chunk, 4))
+        return KV_ERR_INVALID_ARG;
     pv->u_chunk_tok = d->d_u_chunk_tok;
     pv->v_chunk = d->d_v_chunk;
     for (int ch = 0; ch < 2; ++ch) {
@@ -172,6 +178,10 @@ kv_status relocate_impl(const kv_pool_desc *src, const kv_pool_desc *dst, int32_
             return KV_ERR_INVALID_ARG;
         if (num_reqs <= 0 || max_blocks <= 0)
             return KV_ERR_INVALID_ARG;
+        const void *i32s[6] = {tok_off, src_slots, chunk_req, chunk_dst_pos, delta, block_tables};
+        for (const void *a : i32s)
+            if (!aligned_to(a, 4))
+                return KV_ERR_INVALID_ARG;
     }
     PatchView pv;
     bool patched = false;
@@ -503,7 +513,7 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
             h_seq_lens[q] = h_s_start[q];
         return KV_OK;
     }
-    if (!d_block_tables || max_blocks <= 0)
+    if (!d_block_tables || !aligned_to(d_block_tables, 4) || max_blocks <= 0)
         return KV_ERR_INVALID_ARG;
     if (total_stub > 0 && (!d_stub_copy || !d_stub_rot || !aligned16(d_stub_copy) ||
                            !aligned16(d_stub_rot)))
@@ -713,7 +723,8 @@ kv_status kv_splice_composed(const kv_pool_desc *pool, int32_t num_seqs, int32_t
         return KV_ERR_INVALID_ARG;
     if (num_seqs == 0 || num_dirs == 0)
         return KV_OK;
-    if (!h_seq_lens || !h_s_start || !h_s_end || !h_stub_len || !d_block_tables || max_blocks <= 0)
+    if (!h_seq_lens || !h_s_start || !h_s_end || !h_stub_len || !d_block_tables ||
+        !aligned_to(d_block_tables, 4) || max_blocks <= 0)
         return KV_ERR_INVALID_ARG;
     ComposedPlan plan;
     kv_status st = plan_composed(kind, num_seqs, num_dirs, (int64_t)max_blocks * pool->block_size,
@@ -838,6 +849,9 @@ kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total
         (max_chunks > 0 && (!d_chunk_end || !d_fingerprint)) ||
         (num_streams == 0 && total_tokens > 0) || cdc_blocks(total_tokens) > 0x7FFFFFFF)
         return KV_ERR_INVALID_ARG;
+    if (!aligned_to(d_stream_off, 8) || !aligned_to(d_tokens, 4) || !aligned_to(d_chunk_end, 8) ||
+        !aligned_to(d_fingerprint, 8) || !aligned_to(d_num_chunks, 8))
+        return KV_ERR_INVALID_ARG;
     kv_status st = ws_ok(d_workspace, workspace_bytes, kv_cdc_workspace_size(total_tokens));
     if (st != KV_OK)
         return st;
@@ -885,6 +899,9 @@ kv_status kv_fingerprint(int64_t num_ranges, const int64_t *d_start, const int64
     t_launches = 0;
     if (num_ranges < 0 || total_tokens < 0 ||
         (num_ranges > 0 && (!d_start || !d_end || !d_fingerprint || (total_tokens > 0 && !d_tokens))))
+        return KV_ERR_INVALID_ARG;
+    if (!aligned_to(d_start, 8) || !aligned_to(d_end, 8) || !aligned_to(d_tokens, 4) ||
+        !aligned_to(d_fingerprint, 8))
         return KV_ERR_INVALID_ARG;
     kv_status st = ws_ok(d_workspace, workspace_bytes, kHeaderBytes);
     if (st != KV_OK)

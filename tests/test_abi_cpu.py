@@ -138,3 +138,23 @@ def test_cdc_host_checks(lib):
                       None) == kv.KV_ERR_WORKSPACE
     assert kv.kv_fingerprint(3, None, None, 10, None, 0, None, ws,
                              check=False) == kv.KV_ERR_INVALID_ARG
+
+
+def test_misaligned_index_arrays_are_rejected(lib):
+    p = _fake_pool()
+    ws = C.c_void_p(1 << 24)
+    ok4, bad4 = C.c_void_p(1 << 20), C.c_void_p((1 << 20) + 2)
+    # an int32 index array not on a 4-byte boundary
+    for i in range(6):
+        args = [ok4] * 6
+        args[i] = bad4
+        tok_off, src_slots, chunk_req, chunk_dst_pos, delta, bt = args
+        assert lib.kv_relocate(C.byref(p), C.byref(p), 1, 10, tok_off, src_slots, chunk_req,
+                               chunk_dst_pos, delta, bt, 1, 1, None, ws, 1 << 20,
+                               None) == kv.KV_ERR_INVALID_ARG
+    # kv_cdc: int64 offsets, int32 tokens
+    ws_t = torch.empty(1 << 12, dtype=torch.uint8)
+    assert kv.kv_cdc(1, C.c_void_p((1 << 20) + 4), 10, ok4, 0, 0, 0, 10, ok4, ok4, ok4, ws_t,
+                     check=False) == kv.KV_ERR_INVALID_ARG
+    assert kv.kv_fingerprint(2, ok4, ok4, 10, bad4, 0, ok4, ws_t,
+                             check=False) == kv.KV_ERR_INVALID_ARG

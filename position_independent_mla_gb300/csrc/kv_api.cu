@@ -627,6 +627,7 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
     std::vector<RemapParams> rplans;
     {
         RemapParams rp{};
+        const int TR = remap_tile_rows(kind);
         int64_t stub_base = 0;
         for (int q = 0; q < num_seqs; ++q) {
             if (remap[q]) {
@@ -641,8 +642,8 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
                 R.n_r = h_stub_len[q];
                 R.delta = R.n_r - (R.s_end - R.s_start);
                 R.bt_row = q;
-                R.n_down = (int32_t)((R.seq_len - R.s_end + T - 1) / T);
-                R.n_stub = (R.n_r + T - 1) / T;
+                R.n_down = (int32_t)((R.seq_len - R.s_end + TR - 1) / TR);
+                R.n_stub = (R.n_r + TR - 1) / TR;
                 R.tile_base = rp.total_tiles;
                 R.stub_base = stub_base;
                 rp.total_tiles += R.n_down + R.n_stub;

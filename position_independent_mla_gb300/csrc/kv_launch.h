@@ -52,4 +52,26 @@ inline int tile_rows(RowKind kind)
     return kTileGqa;
 }
 
+// Rows per tile of the block-table remap's in-place pass over multi-head rows
+// (every byte it moves is rotated): half the rows, four blocks per SM.
+constexpr int kRemapTileGqa = 8;
+constexpr int kRemapTileGqa4 = 16;
+constexpr int kRemapTileMha = 2;
+
+// Rows per tile of the block-table remap (launch_remap).
+inline int remap_tile_rows(RowKind kind)
+{
+    switch (kind) {
+    case RowKind::Mla:
+        return kTileMla;
+    case RowKind::Gqa:
+        return kRemapTileGqa;
+    case RowKind::Gqa4:
+        return kRemapTileGqa4;
+    case RowKind::Mha:
+        return kRemapTileMha;
+    }
+    return kRemapTileGqa;
+}
+
 } // namespace kvr

@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(con
     if (down) {
         // rotary part only, in place; rows of different layers are
         // independent, so LB layers of loads are in flight at once
-        constexpr int LB = G::kRotPer >= 8 ? 1 : 8 / G::kRotPer;
+        constexpr int LB = G::kRotPer >= 4 ? 1 : 8 / G::kRotPer;
         const int Lc = p.pool.num_layers;
         for (int l0 = 0; l0 < Lc; l0 += LB) {
             TileRegs<G> regs[LB];
@@ -462,7 +462,7 @@ cudaError_t launch_remap(const RemapParams &p, RowKind kind, cudaStream_t stream
     if (p.total_tiles > 0) {
         if (p.total_tiles > 0x7FFFFFFFll)
             return cudaErrorInvalidConfiguration;
-        cudaError_t e = with_geo(kind, [&](auto g) {
+        cudaError_t e = with_remap_geo(kind, [&](auto g) {
             return with_bool(p.pool.il != 0, [&](auto il) {
                 remap_data_kernel<typename decltype(g)::type, decltype(il)::value>
                     <<<(unsigned)p.total_tiles, kThreads, 0, stream>>>(p);

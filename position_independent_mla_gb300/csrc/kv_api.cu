@@ -452,7 +452,8 @@ size_t kv_workspace_size(const kv_pool_desc *pool, int64_t max_rows, int32_t max
     RowKind kind;
     if (!pool_ok(pool) || !row_kind(pool, &kind) || max_rows < 0 || max_units < 0)
         return 0;
-    const int64_t T = tile_rows(kind);
+    // the ticketed splice's tiles are the smaller ones (one flag each)
+    const int64_t T = std::min(tile_rows(kind), inplace_tile_rows(kind));
     const int64_t units = std::max<int64_t>(max_units, 1);
     const int64_t flags = (int64_t)pool->num_layers * ((max_rows + T - 1) / T + units);
     return (size_t)kHeaderBytes + table_bytes(pool, units) + align256((size_t)flags * 4u);
@@ -538,7 +539,7 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
                        h_stub_len[q] != h_s_end[q] - h_s_start[q];
 
     // plan: launches of up to kMaxSeqsPerLaunch sequences each
-    const int T = tile_rows(kind);
+    const int T = inplace_tile_rows(kind);
     const int L = pool->num_layers;
     std::vector<SpliceParams> plans;
     int64_t stub_base = 0, max_flags = 0;
@@ -627,7 +628,6 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
     std::vector<RemapParams> rplans;
     {
         RemapParams rp{};
-        const int TR = remap_tile_rows(kind);
         int64_t stub_base = 0;
         for (int q = 0; q < num_seqs; ++q) {
             if (remap[q]) {
@@ -642,8 +642,8 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
                 R.n_r = h_stub_len[q];
                 R.delta = R.n_r - (R.s_end - R.s_start);
                 R.bt_row = q;
-                R.n_down = (int32_t)((R.seq_len - R.s_end + TR - 1) / TR);
-                R.n_stub = (R.n_r + TR - 1) / TR;
+                R.n_down = (int32_t)((R.seq_len - R.s_end + T - 1) / T);
+                R.n_stub = (R.n_r + T - 1) / T;
                 R.tile_base = rp.total_tiles;
                 R.stub_base = stub_base;
                 rp.total_tiles += R.n_down + R.n_stub;

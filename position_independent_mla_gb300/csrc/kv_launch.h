@@ -52,26 +52,27 @@ inline int tile_rows(RowKind kind)
     return kTileGqa;
 }
 
-// Rows per tile of the block-table remap's in-place pass over multi-head rows
-// (every byte it moves is rotated): half the rows, four blocks per SM.
-constexpr int kRemapTileGqa = 8;
-constexpr int kRemapTileGqa4 = 16;
-constexpr int kRemapTileMha = 2;
+// Rows per tile of the in-place passes over multi-head rows (the ticketed
+// splice and the block-table remap): half the rows of the relocation's
+// tiles, at four blocks per SM.
+constexpr int kInPlaceTileGqa = 8;
+constexpr int kInPlaceTileGqa4 = 16;
+constexpr int kInPlaceTileMha = 2;
 
-// Rows per tile of the block-table remap (launch_remap).
-inline int remap_tile_rows(RowKind kind)
+// Rows per tile of launch_splice and launch_remap.
+inline int inplace_tile_rows(RowKind kind)
 {
     switch (kind) {
     case RowKind::Mla:
         return kTileMla;
     case RowKind::Gqa:
-        return kRemapTileGqa;
+        return kInPlaceTileGqa;
     case RowKind::Gqa4:
-        return kRemapTileGqa4;
+        return kInPlaceTileGqa4;
     case RowKind::Mha:
-        return kRemapTileMha;
+        return kInPlaceTileMha;
     }
-    return kRemapTileGqa;
+    return kInPlaceTileGqa;
 }
 
 } // namespace kvr

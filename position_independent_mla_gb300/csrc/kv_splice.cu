@@ -183,7 +183,7 @@ cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stre
     if (p.total_tickets > 0x7FFFFFFFll)
         return cudaErrorInvalidConfiguration;
     const unsigned blocks = (unsigned)p.total_tickets;
-    return with_geo(kind, [&](auto g) {
+    return with_inplace_geo(kind, [&](auto g) {
         return with_bool(p.pool.il != 0, [&](auto il) {
             splice_kernel<typename decltype(g)::type, decltype(il)::value>
                 <<<blocks, kThreads, 0, stream>>>(p);
@@ -462,7 +462,7 @@ cudaError_t launch_remap(const RemapParams &p, RowKind kind, cudaStream_t stream
     if (p.total_tiles > 0) {
         if (p.total_tiles > 0x7FFFFFFFll)
             return cudaErrorInvalidConfiguration;
-        cudaError_t e = with_remap_geo(kind, [&](auto g) {
+        cudaError_t e = with_inplace_geo(kind, [&](auto g) {
             return with_bool(p.pool.il != 0, [&](auto il) {
                 remap_data_kernel<typename decltype(g)::type, decltype(il)::value>
                     <<<(unsigned)p.total_tiles, kThreads, 0, stream>>>(p);

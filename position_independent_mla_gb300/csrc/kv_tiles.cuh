@@ -59,13 +59,14 @@ using GeoGqa4 = Geo<kTileGqa4, 64, 4, 8, 2>;
 // MHA rows: V 32x128 + K 32x128 (Llama-2-7B shape).
 using GeoMha = Geo<kTileMha, 512, 32, 8, 2>;
 
-// The block-table remap's in-place pass turns every byte it moves, so its
-// limit is arithmetic latency rather than bytes in flight: multi-head rows
-// take tiles of half the rows there, four vectors per thread and four
-// blocks (32 warps) per SM.
-using GeoGqaRemap = Geo<kRemapTileGqa, 128, 8, 8, 4>;
-using GeoGqa4Remap = Geo<kRemapTileGqa4, 64, 4, 8, 4>;
-using GeoMhaRemap = Geo<kRemapTileMha, 512, 32, 8, 4>;
+// The in-place passes (the ticketed splice, the block-table remap) are
+// limited by latency -- the rotation's dependent arithmetic, the splice's
+// waits -- rather than by bytes in flight: multi-head rows take tiles of
+// half the rows there, four rotary vectors per thread and four blocks
+// (32 warps) per SM.
+using GeoGqaInPlace = Geo<kInPlaceTileGqa, 128, 8, 8, 4>;
+using GeoGqa4InPlace = Geo<kInPlaceTileGqa4, 64, 4, 8, 4>;
+using GeoMhaInPlace = Geo<kInPlaceTileMha, 512, 32, 8, 4>;
 
 // Multi-head rows (GQA, MHA: rotation is half of every row) without a
 // patch term, in rotate-half pairing, take the pair-packed rotation; the
@@ -120,19 +121,19 @@ cudaError_t with_geo(RowKind kind, F &&f)
     return cudaErrorInvalidValue;
 }
 
-// with_geo for the block-table remap (tile rows as remap_tile_rows).
+// with_geo for the in-place passes (tile rows as inplace_tile_rows).
 template <class F>
-cudaError_t with_remap_geo(RowKind kind, F &&f)
+cudaError_t with_inplace_geo(RowKind kind, F &&f)
 {
     switch (kind) {
     case RowKind::Mla:
         return f(GeoTag<GeoMla>{});
     case RowKind::Gqa:
-        return f(GeoTag<GeoGqaRemap>{});
+        return f(GeoTag<GeoGqaInPlace>{});
     case RowKind::Gqa4:
-        return f(GeoTag<GeoGqa4Remap>{});
+        return f(GeoTag<GeoGqa4InPlace>{});
     case RowKind::Mha:
-        return f(GeoTag<GeoMhaRemap>{});
+        return f(GeoTag<GeoMhaInPlace>{});
     }
     return cudaErrorInvalidValue;
 }

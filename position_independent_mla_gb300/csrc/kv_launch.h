@@ -36,7 +36,7 @@ cudaError_t launch_cdc(const CdcParams &p, cudaStream_t stream);
 cudaError_t launch_fingerprint(const FingerprintParams &p, cudaStream_t stream);
 constexpr int kCdcLaunches = 3;
 
-// Rows per tile of each kind (splice workspace sizing).
+// Rows per tile of each kind for the relocation and the composed splice.
 inline int tile_rows(RowKind kind)
 {
     switch (kind) {

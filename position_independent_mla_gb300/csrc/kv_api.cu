@@ -314,7 +314,7 @@ kv_status plan_composed(RowKind kind, int32_t num_seqs, int32_t num_dirs, int64_
                         const int32_t *lens, const int32_t *s0, const int32_t *s1,
                         const int32_t *nr, ComposedPlan &plan)
 {
-    const int64_t T = tile_rows(kind);
+    const int64_t T = inplace_tile_rows(kind);
     // validate every directive in the indexing the previous ones leave
     plan.total_stub = 0;
     for (int32_t q = 0; q < num_seqs; ++q) {
@@ -452,7 +452,7 @@ size_t kv_workspace_size(const kv_pool_desc *pool, int64_t max_rows, int32_t max
     RowKind kind;
     if (!pool_ok(pool) || !row_kind(pool, &kind) || max_rows < 0 || max_units < 0)
         return 0;
-    // the ticketed splice's tiles are the smaller ones (one flag each)
+    // the splices' tiles are the smaller ones (one flag each)
     const int64_t T = std::min(tile_rows(kind), inplace_tile_rows(kind));
     const int64_t units = std::max<int64_t>(max_units, 1);
     const int64_t flags = (int64_t)pool->num_layers * ((max_rows + T - 1) / T + units);

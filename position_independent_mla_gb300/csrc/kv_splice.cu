@@ -308,7 +308,7 @@ cudaError_t launch_splice_composed(const ComposedParams &p, RowKind kind, cudaSt
     if (p.num_tiles > 0x7FFFFFFFll)
         return cudaErrorInvalidConfiguration;
     const unsigned blocks = (unsigned)p.num_tiles;
-    return with_geo(kind, [&](auto g) {
+    return with_inplace_geo(kind, [&](auto g) {
         return with_bool(p.pool.il != 0, [&](auto il) {
             splice_composed_kernel<typename decltype(g)::type, decltype(il)::value>
                 <<<blocks, kThreads, 0, stream>>>(p);

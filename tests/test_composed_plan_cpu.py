@@ -74,7 +74,7 @@ def _check_plan(kind, lens, dirs):
     tl, s0, s1, nr = _tensors(lens, dirs)
     st, tiles, deltas = kv.kv_splice_composed_plan(_desc(kind), tl, s0, s1, nr)
     assert st == kv.KV_OK
-    T = 32 if kind == "mla" else 16
+    T = 32 if kind == "mla" else 8
     seqs = _origins(lens, dirs)
     covered = {}
     for t, tile in enumerate(tiles):

@@ -3,27 +3,38 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--check]
 
-Default workload (the one the headline metric is quoted on): Irminsul-style
-relocation with a DeepSeek-V3-shaped MLA cache -- 61 layers, rows of c_KV 512
-+ k_pe 64 bf16, 64-token blocks, 32 requests each assembling 16 chunks (lengths
-uniform in 256..2048 tokens) from a registry of 256 canonical chunks, δ per
-chunk uniform in [-32768, 32768].  One step = one kv_relocate call (δ-table
-kernel + relocation kernel) over the whole batch.  Other workloads:
-``splice-mla-128k`` (Leyline AMORTIZE at 128K context), ``relocate-gqa-patch``
-(Kamera GQA with a fused rank-16 patch), ``splice-mla-4k`` (one layer, 4096
-tokens).
+With no --workload, every configured workload prints one JSON line (rank 0),
+in this order, the headline last:
+  splice-mla-4k       Leyline splice on one MLA layer of 4096 tokens,
+                      [1024, 2048) -> 16-row stub (L2-resident);
+  splice-mla-128k     Leyline AMORTIZE at 128K context: 61 layers, 8 sequences
+                      of 131072 tokens, 4 successive directives each;
+  relocate-gqa-patch  Kamera GQA relocation (32 layers, 8 x 128 K and V) with
+                      a fused rank-16 patch on K and V;
+  sweep-mla           MLA relocation over chunk lengths 16..4096 x δ in
+                      {±1, ±1000, ±100000}, the splice with Δ = δ and the
+                      standalone rank-8 patch (one summary line);
+  relocate-mla        the headline: Irminsul-style relocation with a
+                      DeepSeek-V3-shaped MLA cache -- 61 layers, rows of c_KV
+                      512 + k_pe 64 bf16, 64-token blocks, 32 requests each
+                      assembling 16 chunks (U[256, 2048] tokens) from a
+                      256-chunk registry, δ U[-32768, 32768]; one step = one
+                      kv_relocate call (δ-table + relocation kernels).
+Other workloads (--workload): relocate-mla-patch, splice-mla-128k-composed,
+splice-mla-128k-remap (and -split), window-gqa, families, cdc-tokens.
 
-Prints one JSON line (rank 0).  ``value`` is relocated KV tokens/s over all
-layers for the whole job; ``roofline`` gives the dominant kernel's achieved
-HBM bandwidth (algorithmic bytes / CUDA-event time on its stream) against the
-measured copy peak; ``e2e`` is the same metric through the C-ABI call with the
-per-step index arrays copied from pinned host memory and the status word
-read back every step; ``cpu_baseline`` is the fp64 oracle timed on a bounded
-sample of the same workload on the host cores.
+``value`` is the workload's metric for the whole job (relocated KV tokens/s
+over all layers); ``roofline`` gives the dominant kernel's achieved HBM
+bandwidth (algorithmic bytes per launch / CUDA-event time on its stream)
+against the measured copy peak; ``e2e`` is the same metric through the C-ABI
+call with the step's inputs copied from pinned host memory and the status
+word read back every step; ``cpu_baseline`` is the fp64 oracle timed on
+bounded samples of the same recipe on every host core and on one core.
 """
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -281,35 +292,94 @@ def check_relocate_sample(st, orc, n_rows: int = 3000, seed: int = 7) -> dict:
             "rot_one_ulp": r["one_ulp"], "rot_beyond": r["beyond"]}
 
 
-def cpu_baseline_relocate(orc, cfg=RELOC_MLA, chunks: int = 3, seed: int = 4242,
-                          min_seconds: float = 10.0):
-    """Oracle relocation of a bounded sample: 1 request x `chunks` chunks drawn
-    with the workload's recipe, all layers, KV values drawn on the host; the
-    call is repeated until at least `min_seconds` of CPU work is timed."""
+# ---------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle, as it stands, on bounded samples of each
+# workload's recipe, timed on one host core and on every host core at once
+# (one spawned process per core, each on its own independent sample; the
+# oracle's arithmetic is unchanged)
+# ---------------------------------------------------------------------------
+
+def _mla_pool(O, L, slots, seed, base=10000.0):
+    return O.Pool(synth.bits(synth.bf16_normal((L, slots, 512), seed)).copy(),
+                  synth.bits(synth.bf16_normal((L, slots, 64), seed + 1)).copy(), 64, 1, 64, base)
+
+
+def oracle_sample(kind: str, n: int, seed: int):
+    """One bounded oracle sample of workload `kind` (size parameter `n`):
+    returns (call, units, what) -- `call()` runs the oracle once, `units` is
+    the metric's units one call yields (rows or tokens moved, all layers),
+    `what` describes the sample."""
     import oracle as O
 
-    c = cfg
-    wl = synth.relocate_workload(seed, num_reqs=1, chunks_per_req=chunks, len_lo=c["len_lo"],
-                                 len_hi=c["len_hi"], delta_lo=c["delta_lo"],
-                                 delta_hi=c["delta_hi"], n_pool_chunks=chunks, base_hi=63)
-    L = c["layers"]
-    src = O.Pool(synth.bits(synth.bf16_normal((L, wl.src_slots_total, 512), seed)).copy(),
-                 synth.bits(synth.bf16_normal((L, wl.src_slots_total, 64), seed + 1)).copy(),
-                 64, 1, 64, c["base"])
-    dst = O.Pool(np.zeros((L, wl.dst_slots_total, 512), np.uint16),
-                 np.zeros((L, wl.dst_slots_total, 64), np.uint16), 64, 1, 64, c["base"])
-    reps, dt = 0, 0.0
-    while reps < 1000 and (dt < min_seconds or reps == 0):
-        t0 = time.perf_counter()
-        assert orc.relocate(src, dst, wl.tok_off, wl.src_slots, wl.chunk_req,
-                            wl.chunk_dst_pos, wl.delta, wl.block_tables) == O.OK
-        dt += time.perf_counter() - t0
-        reps += 1
-    return wl.total_tokens * reps, dt, wl.total_tokens, reps
+    orc = O.get()
+    if kind in ("relocate-mla", "sweep-mla"):
+        c = RELOC_MLA
+        if kind == "relocate-mla":   # one chunk of n tokens, the headline's δ range
+            wl = synth.relocate_workload(seed, num_reqs=1, chunks_per_req=1, len_lo=n, len_hi=n,
+                                         delta_lo=c["delta_lo"], delta_hi=c["delta_hi"],
+                                         n_pool_chunks=1, base_hi=63)
+            what = f"one {n}-token chunk, 61 layers"
+        else:                        # 8n short chunks over the sweep's range of shifts
+            wl = synth.relocate_workload(seed, num_reqs=1, chunks_per_req=8 * n, len_lo=16,
+                                         len_hi=256, delta_lo=-100000, delta_hi=100000,
+                                         n_pool_chunks=8 * n, base_hi=63)
+            what = f"one request of {8 * n} chunks of U[16,256] tokens, 61 layers"
+        L = c["layers"]
+        src = _mla_pool(O, L, wl.src_slots_total, seed)
+        dst = O.Pool(np.zeros((L, wl.dst_slots_total, 512), np.uint16),
+                     np.zeros((L, wl.dst_slots_total, 64), np.uint16), 64, 1, 64, c["base"])
 
+        def call():
+            assert orc.relocate(src, dst, wl.tok_off, wl.src_slots, wl.chunk_req,
+                                wl.chunk_dst_pos, wl.delta, wl.block_tables) == O.OK
+        return call, wl.total_tokens, what
+    if kind == "relocate-gqa-patch":   # n chunks of 576 tokens, rank-16 patch on K and V
+        c = RELOC_GQA
+        wl = synth.relocate_workload(seed, num_reqs=1, chunks_per_req=n, len_lo=c["chunk_len"],
+                                     len_hi=c["chunk_len"], delta_lo=c["delta_lo"],
+                                     delta_hi=c["delta_hi"], n_pool_chunks=n, base_hi=63)
+        L, m = c["layers"], c["rank"]
+        src = O.Pool(synth.bits(synth.bf16_normal((L, wl.src_slots_total, 1024), seed)).copy(),
+                     synth.bits(synth.bf16_normal((L, wl.src_slots_total, 1024), seed + 1)).copy(),
+                     64, 8, 128, c["base"])
+        dst = O.Pool(np.zeros((L, wl.dst_slots_total, 1024), np.uint16),
+                     np.zeros((L, wl.dst_slots_total, 1024), np.uint16), 64, 8, 128, c["base"])
+        u = [synth.f32_normal((L, wl.total_tokens, m), seed + 2 + i, std=c["std"]).numpy()
+             for i in range(2)]
+        v = [synth.f32_normal((L, wl.num_chunks, 1024, m), seed + 4 + i, std=c["std"]).numpy()
+             for i in range(2)]
+        patch = O.Patch(m, u, v)
 
-# ---- the oracle on every host core: one spawned process per core, each on its
-# own independent sample (requests are independent units of the relocation) ----
+        def call():
+            assert orc.relocate(src, dst, wl.tok_off, wl.src_slots, wl.chunk_req,
+                                wl.chunk_dst_pos, wl.delta, wl.block_tables, patch) == O.OK
+        return call, wl.total_tokens, f"{n} chunk(s) of 576 tokens, 32 layers, rank-16 patch"
+    if kind in ("splice-mla-128k", "splice-mla-4k"):
+        if kind == "splice-mla-4k":    # the whole configured case: 1 layer, 4096 tokens
+            c = SPLICE_4K
+            L, seq = 1, c["seq_len"]
+            s0, s1, nr = c["s_start"], c["s_end"], c["stub"]
+            what = "the whole case (1 layer, 4096 tokens, [1024,2048) -> 16 rows)"
+        else:                          # one n-token sequence, one directive, all 61 layers
+            c = SPLICE_128K
+            L, seq = c["layers"], n
+            d = synth.random_directives(seed, [seq], seq // 16, seq // 4, c["stub_lo"],
+                                        c["stub_hi"])
+            s0, s1, nr = int(d.s_start[0]), int(d.s_end[0]), int(d.stub_len[0])
+            what = (f"one {seq}-token sequence, 61 layers, one directive removing {s1 - s0} "
+                    f"tokens for a {nr}-row stub")
+        ss = synth.splice_seqs(seed, [seq], (seq + 63) // 64)
+        pool = _mla_pool(O, L, ss.num_slots, seed, c["base"])
+        sc = synth.bits(synth.bf16_normal((L, nr, 512), seed + 2)).copy()
+        sr = synth.bits(synth.bf16_normal((L, nr, 64), seed + 3)).copy()
+        moved = (seq - s1) + nr
+
+        def call():
+            lens = np.array([seq], np.int32)
+            assert orc.splice(pool, ss.block_tables, lens, [s0], [s1], [nr], sc, sr) == O.OK
+        return call, moved, what
+    raise ValueError(kind)
+
 
 _CORE_BARRIER = None
 
@@ -320,31 +390,19 @@ def _core_init(barrier):
     torch.set_num_threads(1)  # one core per process, also while drawing the sample
 
 
-def _core_task(n_tok: int, seed: int, min_seconds: float):
-    """One core's share: build a one-chunk sample of `n_tok` tokens (untimed),
-    wait for every core, then relocate it until `min_seconds` have passed.
-    Returns (tokens, start, end) on the system-wide monotonic clock."""
-    import oracle as O
-
-    orc = O.get()
-    c = RELOC_MLA
-    wl = synth.relocate_workload(seed, num_reqs=1, chunks_per_req=1, len_lo=n_tok, len_hi=n_tok,
-                                 delta_lo=c["delta_lo"], delta_hi=c["delta_hi"], n_pool_chunks=1,
-                                 base_hi=63)
-    L = c["layers"]
-    src = O.Pool(synth.bits(synth.bf16_normal((L, wl.src_slots_total, 512), seed)).copy(),
-                 synth.bits(synth.bf16_normal((L, wl.src_slots_total, 64), seed + 1)).copy(),
-                 64, 1, 64, c["base"])
-    dst = O.Pool(np.zeros((L, wl.dst_slots_total, 512), np.uint16),
-                 np.zeros((L, wl.dst_slots_total, 64), np.uint16), 64, 1, 64, c["base"])
-    _CORE_BARRIER.wait(timeout=600)
+def _core_task(kind: str, n: int, seed: int, min_seconds: float):
+    """One core's share: build its sample (untimed), wait for every core, then
+    run the oracle on it until `min_seconds` have passed.  Returns (units,
+    start, end, what) on the system-wide monotonic clock."""
+    call, units, what = oracle_sample(kind, n, seed)
+    if _CORE_BARRIER is not None:
+        _CORE_BARRIER.wait(timeout=600)
     t0 = time.monotonic()
     reps = 0
     while reps == 0 or time.monotonic() - t0 < min_seconds:
-        assert orc.relocate(src, dst, wl.tok_off, wl.src_slots, wl.chunk_req, wl.chunk_dst_pos,
-                            wl.delta, wl.block_tables) == O.OK
+        call()
         reps += 1
-    return wl.total_tokens * reps, t0, time.monotonic()
+    return units * reps, t0, time.monotonic(), what
 
 
 class OracleCores:
@@ -360,13 +418,13 @@ class OracleCores:
         self.pool = cf.ProcessPoolExecutor(self.n, mp_context=ctx, initializer=_core_init,
                                            initargs=(ctx.Barrier(self.n),))
 
-    def run(self, n_tok: int, seed: int, min_seconds: float = 0.0):
-        """Every core relocates its own `n_tok`-token sample; returns (tokens, seconds)
-        with seconds from the first start to the last end."""
-        futs = [self.pool.submit(_core_task, n_tok, seed + 7919 * i, min_seconds)
+    def run(self, kind: str, n: int, seed: int, min_seconds: float = 0.0):
+        """Every core runs its own sample of `kind`; returns (units, seconds,
+        what) with seconds from the first start to the last end."""
+        futs = [self.pool.submit(_core_task, kind, n, seed + 7919 * i, min_seconds)
                 for i in range(self.n)]
         res = [f.result() for f in futs]
-        return sum(r[0] for r in res), max(r[2] for r in res) - min(r[1] for r in res)
+        return sum(r[0] for r in res), max(r[2] for r in res) - min(r[1] for r in res), res[0][3]
 
     def close(self):
         self.pool.shutdown()
@@ -384,16 +442,33 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def cpu_baseline_all_cores(n_tok: int = 512, min_seconds: float = 10.0):
-    """The oracle on every host core at once, each core on its own one-chunk
-    sample of `n_tok` tokens (all layers), for at least `min_seconds`."""
-    cores = OracleCores()
+# Sample size per core and per single-thread run of each workload's oracle
+# baseline, and the seconds each is timed for.
+CPU_SAMPLES = {"relocate-mla": (512, 4096, 10.0), "sweep-mla": (1, 2, 4.0),
+               "relocate-gqa-patch": (1, 1, 4.0), "splice-mla-128k": (4096, 8192, 4.0),
+               "splice-mla-4k": (0, 0, 4.0)}
+
+
+def cpu_baseline(kind: str, unit: str, cores: "OracleCores | None" = None) -> dict:
+    """The oracle on every host core at once and on one core, on bounded
+    samples of `kind`'s recipe."""
+    n_all, n_one, secs = CPU_SAMPLES[kind]
+    own = cores is None
+    if own:
+        cores = OracleCores()
     try:
-        cores.run(16, 1, 0.0)  # spawn and import everywhere before the timed round
-        ntok, dt = cores.run(n_tok, 9001, min_seconds)
+        cores.run("splice-mla-4k", 0, 1, 0.0)   # spawn and import everywhere, untimed
+        units, dt, what = cores.run(kind, n_all, 9001, secs)
     finally:
-        cores.close()
-    return ntok, dt, cores.n
+        if own:
+            cores.close()
+    u1, t0, t1, what1 = _core_task(kind, n_one, 4242, secs)
+    return {"value": units / dt, "unit": unit, "cores": cores.n, "kind": "oracle",
+            "cpu": cpu_model(),
+            "sample": f"{cores.n} processes side by side, each on its own sample ({what}) "
+                      f"for {dt:.1f} s",
+            "single_thread": {"value": u1 / (t1 - t0), "unit": unit, "cores": 1,
+                              "sample": f"{what1}, repeated for {t1 - t0:.1f} s"}}
 
 
 # A small case of the same kernel for ncu captures (a few GB on the device).
@@ -457,12 +532,9 @@ def run_relocate_mla(args, rank, world, local):
     total_tokens = tokens * world  # weak scaling: every rank relocates its own batch
 
     check = None
-    orc = None
-    if rank == 0 and (args.check or not args.no_cpu_baseline):
-        import oracle as O
-        orc = O.get()
     if args.check and rank == 0:
-        check = check_relocate_sample(st, orc)
+        import oracle as O
+        check = check_relocate_sample(st, O.get())
 
     bytes_per_launch = tokens * (L * 2 * MLA_ROW_BYTES + 4)
     peak, peak_kind = hbm_peak()
@@ -494,19 +566,6 @@ def run_relocate_mla(args, rank, world, local):
         "clocks": clk,
         "gpu_launches": launches,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        ntok, dt, per, reps = cpu_baseline_relocate(orc)
-        atok, adt, ncores = cpu_baseline_all_cores()
-        out["cpu_baseline"] = {"value": atok / adt, "unit": "tokens/s", "cores": ncores,
-                               "kind": "oracle", "cpu": cpu_model(),
-                               "sample": f"{ncores} processes side by side, each relocating its "
-                                         f"own 512-token chunk of the same recipe (all 61 "
-                                         f"layers) for {adt:.1f} s",
-                               "single_thread": {
-                                   "value": ntok / dt, "unit": "tokens/s", "cores": 1,
-                                   "sample": f"1 request x 3 chunks ({per} tokens) of the same "
-                                             f"recipe, all 61 layers, relocated {reps} times: "
-                                             f"{dt:.1f} s"}}
     if check is not None:
         out["parity_sample"] = check
     return out
@@ -630,17 +689,46 @@ SPLICE_128K = dict(layers=61, num_seqs=8, seq_len=131072, rounds=4, span_lo=8192
 SPLICE_128K_SMALL = dict(SPLICE_128K, num_seqs=1, seq_len=32768, span_lo=2048, span_hi=8192)
 
 
-def build_splice(rank: int, cfg, device: str = "cuda", aligned: bool = False):
+class SplitPool:
+    """An MLA pool stored as two tensors, c_KV [L][slots][512] and k_pe
+    [L][slots][64]; indexing returns the joined 576-wide rows."""
+
+    def __init__(self, c: torch.Tensor, r: torch.Tensor):
+        self.c, self.r = c, r
+
+    def __getitem__(self, idx):
+        return torch.cat([self.c[idx], self.r[idx]], -1)
+
+    def copy_(self, other: "SplitPool"):
+        self.c.copy_(other.c)
+        self.r.copy_(other.r)
+        return self
+
+    def clone(self) -> "SplitPool":
+        return SplitPool(self.c.clone(), self.r.clone())
+
+
+def build_splice(rank: int, cfg, device: str = "cuda", aligned: bool = False,
+                 split: bool = False):
+    """The 128K-context splice workload.  `split`: the pool as separate c_KV
+    and k_pe tensors instead of one [L][slots][576] tensor."""
     import position_independent_mla_gb300 as kv
 
     c = cfg
     L, S, n = c["layers"], c["num_seqs"], c["seq_len"]
     max_blocks = (n + 63) // 64          # spans (>= 8K) outgrow stubs: sequences shrink
     ss = synth.splice_seqs(3003 + 100 * rank, [n] * S, max_blocks)
-    pool = torch.empty((L, ss.num_slots, MLA_ROW), dtype=torch.bfloat16, device=device)
-    fill_normal_(pool, 3003 + 100 * rank)
+    if split:
+        pool = SplitPool(torch.empty((L, ss.num_slots, 512), dtype=torch.bfloat16, device=device),
+                         torch.empty((L, ss.num_slots, 64), dtype=torch.bfloat16, device=device))
+        fill_normal_(pool.c, 3003 + 100 * rank)
+        fill_normal_(pool.r, 3053 + 100 * rank)
+        desc = kv.pool_desc(pool.c, pool.r, 64, 1, c["base"])
+    else:
+        pool = torch.empty((L, ss.num_slots, MLA_ROW), dtype=torch.bfloat16, device=device)
+        fill_normal_(pool, 3003 + 100 * rank)
+        desc = kv.pool_desc(pool[..., :512], pool[..., 512:], 64, 1, c["base"])
     pristine = pool.clone()
-    desc = kv.pool_desc(pool[..., :512], pool[..., 512:], 64, 1, c["base"])
     lens = ss.seq_lens.copy()
     rounds = []
     for r in range(c["rounds"]):
@@ -786,15 +874,22 @@ def run_splice_mla_128k(args, rank, world, local):
     step_ms = sum(a.elapsed_time(b) for a, b in step_ev) / K
     kern_ms = sum(a.elapsed_time(b) for a, b in kern_ev) / K
 
-    # end to end: the directive arguments are host arrays by design; each step
-    # restores (untimed), then times the calls and a status read-back per round
+    # end to end: each step restores the cache (untimed), then times, per
+    # round, the copy of the prefilled stub rows from pinned host memory, the
+    # call (the directive arguments are host arrays by design) and a status
+    # read-back
+    host_stubs = [(rd["stub_c"].cpu().pin_memory(), rd["stub_r"].cpu().pin_memory())
+                  for rd in st["rounds"]]
+    stub_bytes = sum(a.numel() * 2 + b.numel() * 2 for a, b in host_stubs)
     e2e_s = 0.0
     for k in range(K):
         st["pool"].copy_(st["pristine"])
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         lens = torch.from_numpy(st["ss"].seq_lens.copy())
-        for rd in st["rounds"]:
+        for rd, (hc, hr) in zip(st["rounds"], host_stubs):
+            rd["stub_c"].copy_(hc, non_blocking=True)
+            rd["stub_r"].copy_(hr, non_blocking=True)
             s0, s1, nr = rd["args"]
             kv.kv_splice(st["desc"], st["S"], st["bt"], st["max_blocks"], lens, s0, s1, nr,
                          rd["stub_c"], rd["stub_r"], kv.KV_AMORTIZE, st["ws"])
@@ -827,9 +922,14 @@ def run_splice_mla_128k(args, rank, world, local):
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": recorded_traffic("splice_mla_128k"),
                      "kernel": "splice_kernel<MLA>", "kernel_ms": kern_ms,
+                     "launches_per_step": R, "kernel_ms_per_launch": kern_ms / R,
+                     "algorithmic_bytes_per_launch": bytes_per_step / R,
                      "algorithmic_bytes_per_step": bytes_per_step},
         "e2e": {"value": moved * world * K / e2e_s, "unit": "tokens/s",
-                "h2d_bytes_per_step": 16 * st["S"] * R, "d2h_bytes_per_step": 4 * R},
+                "h2d_bytes_per_step": stub_bytes + 12 * st["S"] * R,
+                "d2h_bytes_per_step": 4 * R,
+                "copies": "per round: the stub rows from pinned host memory; the directive "
+                          "(3 int32 per sequence) goes by value in the launch"},
         "clocks": clk, "gpu_launches": launches,
     }
     if args.check and rank == 0:
@@ -838,17 +938,20 @@ def run_splice_mla_128k(args, rank, world, local):
     return out
 
 
-def run_splice_mla_128k_remap(args, rank, world, local):
+def run_splice_mla_128k_remap(args, rank, world, local, split: bool = False):
     """The 128K-context workload with block-aligned directives (spans of
     U[8192, 32768] tokens rounded to whole blocks at block-aligned offsets,
     stubs of 1-4 blocks), applied with KV_AMORTIZE_REMAP: downstream rows stay
     in their blocks, the block-table rows are permuted and only the rotary
     part is rewritten.  Timed against KV_AMORTIZE on the same directives;
-    before each step the cache and the block tables are restored, untimed."""
+    before each step the cache and the block tables are restored, untimed.
+    `split`: c_KV and k_pe in separate tensors, so the rotary part of
+    consecutive slots is contiguous (128 B rows) instead of 128 B out of every
+    1152 B row of a fused pool."""
     import position_independent_mla_gb300 as kv
 
     cfg = SPLICE_128K_SMALL if args.small else SPLICE_128K
-    st = build_splice(rank, cfg, aligned=True)
+    st = build_splice(rank, cfg, aligned=True, split=split)
     L, R, S, K, W = st["L"], len(st["rounds"]), st["S"], args.steps, args.warmup
     bt0 = st["bt"].clone()
 
@@ -880,7 +983,9 @@ def run_splice_mla_128k_remap(args, rank, world, local):
         "config": {"workload": f"leyline-splice-mla-remap: {L} layers, {S} sequences x "
                                f"{cfg['seq_len']} tokens, {R} block-aligned directives (spans of "
                                f"U[{cfg['span_lo']},{cfg['span_hi']}] tokens in whole blocks, "
-                               "stubs of 1-4 blocks) applied by block-table remapping",
+                               "stubs of 1-4 blocks) applied by block-table remapping; pool "
+                               + ("split: c_KV [L][slots][512] and k_pe [L][slots][64]" if split
+                                  else "fused: [L][slots][576]"),
                    "rows_moved_per_step_per_gpu": moved, "downstream_rows": down,
                    "stub_rows": stub, "layers": L, "amortize_ms": amortize_ms,
                    "speedup_vs_amortize": amortize_ms / ms,
@@ -889,7 +994,7 @@ def run_splice_mla_128k_remap(args, rank, world, local):
                          "tables restored before each step, untimed" % (nbytes / 1e9)},
         "roofline": {"bound": "hbm", "achieved": nbytes / (kms * 1e-3) / 1e9 if kms > 0 else None,
                      "peak": peak, "unit": "GB/s", "peak_kind": peak_kind,
-                     "traffic": recorded_traffic("splice_mla_128k_remap"),
+                     "traffic": (None if split else recorded_traffic("splice_mla_128k_remap")),
                      "kernel": "remap_data_kernel<MLA> (whole step: 4 rounds)",
                      "kernel_ms_last_round": kms, "algorithmic_bytes_per_step": nbytes,
                      "frac": None},
@@ -1257,6 +1362,23 @@ def run_splice_mla_4k(args, rank, world, local):
             launches += one(cold, e)
         torch.cuda.synchronize()
         res["cold" if cold else "warm"] = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    # end to end through the C ABI: per step the stub rows come from pinned
+    # host memory, then the call and a status read-back (cache restored and
+    # L2 flushed before each step, untimed)
+    hc, hr = stub_c.cpu().pin_memory(), stub_r.cpu().pin_memory()
+    e2e_s = 0.0
+    for _ in range(args.steps):
+        pool.copy_(pristine)
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        stub_c.copy_(hc, non_blocking=True)
+        stub_r.copy_(hr, non_blocking=True)
+        lens = torch.tensor([c["seq_len"]], dtype=torch.int32)
+        kv.kv_splice(desc, 1, bt, ss.block_tables.shape[1], lens, s0, s1, nr, stub_c, stub_r,
+                     kv.KV_AMORTIZE, ws)
+        assert kv.kv_get_device_status(ws) == kv.KV_OK
+        e2e_s += time.perf_counter() - t0
     clk = clocks.stop()
     assert kv.kv_get_device_status(ws) == kv.KV_OK
     bytes_step = moved * 2 * MLA_ROW_BYTES
@@ -1273,10 +1395,18 @@ def run_splice_mla_4k(args, rank, world, local):
                          "before each step, untimed); warm given beside it",
                    "warm_ms": res["warm"], "cold_ms": res["cold"],
                    "warm_tokens_per_s": moved / (res["warm"] * 1e-3)},
-        "roofline": {"bound": "latency", "achieved": bytes_step / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": bytes_step / (ms * 1e-3) / 1e9,
                      "peak": peak, "unit": "GB/s", "frac": bytes_step / (ms * 1e-3) / 1e9 / peak,
                      "peak_kind": peak_kind, "traffic": None, "kernel": "splice_kernel<MLA>",
-                     "kernel_ms": ms, "algorithmic_bytes_per_step": bytes_step},
+                     "kernel_ms": ms, "algorithmic_bytes_per_launch": bytes_step,
+                     "note": "4.7 MB edit: one wave of 65 blocks, bound by launch and "
+                             "per-block latency, not by HBM bandwidth; the fraction is "
+                             "reported against the HBM copy peak for form"},
+        "e2e": {"value": moved * world * args.steps / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(hc.numel() * 2 + hr.numel() * 2),
+                "d2h_bytes_per_step": 4,
+                "copies": "the stub rows from pinned host memory; the directive goes by value "
+                          "in the launch"},
         "clocks": clk, "gpu_launches": launches,
     }
     return out
@@ -1312,12 +1442,12 @@ def run_reference(args, rank, world):
     per_core = int(max(16, min(4096, rate * 120.0 / max(1, args.steps + args.warmup))))
     cores = OracleCores()  # one process per host core, spawned before any timing
     try:
-        cores.run(16, 1)
+        cores.run("relocate-mla", 16, 1)
         for w in range(args.warmup):
-            cores.run(per_core, 10 + w)
+            cores.run("relocate-mla", per_core, 10 + w)
         total, ntok = 0.0, 0
         for k in range(args.steps):
-            n, dt = cores.run(per_core, 1000 + 131 * k)
+            n, dt, _ = cores.run("relocate-mla", per_core, 1000 + 131 * k)
             ntok += n
             total += dt
     finally:
@@ -1660,9 +1790,10 @@ def run_sweep_mla(args, rank, world, local):
         for j, delta in enumerate(cfg["deltas"]):
             wl = synth.fixed_chunk_workload(5100 + 100 * rank + 10 * i + j, cl, delta, R, N)
             wls.setdefault(cl, wl)
-            d = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).cuda()
-                 for k in ("tok_off", "src_slots", "chunk_req", "chunk_dst_pos", "delta",
-                           "block_tables")}
+            host = {k: torch.from_numpy(np.ascontiguousarray(getattr(wl, k))).pin_memory()
+                    for k in ("tok_off", "src_slots", "chunk_req", "chunk_dst_pos", "delta",
+                              "block_tables")}
+            d = {k: v.cuda() for k, v in host.items()}
             ws = kv.workspace(dd, wl.total_tokens, wl.num_chunks)
 
             def call(wl=wl, d=d, ws=ws):
@@ -1674,12 +1805,23 @@ def run_sweep_mla(args, rank, world, local):
             ms, kms, n = _timed(call, K, W)
             launches += n
             assert kv.kv_get_device_status(ws) == kv.KV_OK
+            # end to end: the index arrays from pinned host memory, the call, a
+            # status read-back
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(K):
+                for k2 in host:
+                    d[k2].copy_(host[k2], non_blocking=True)
+                call()
+                assert kv.kv_get_device_status(ws) == kv.KV_OK
+            e2e_ms = (time.perf_counter() - t0) / K * 1e3
             T = wl.total_tokens
             nbytes = T * (L * 2 * MLA_ROW_BYTES + 4)
             pt = {"chunk_len": cl, "delta": delta, "chunks": wl.num_chunks, "ms": ms,
                   "kernel_ms": kms, "tokens_per_s": T / (ms * 1e-3),
                   "gbs": nbytes / (kms * 1e-3) / 1e9, "frac": nbytes / (kms * 1e-3) / 1e9 / peak,
-                  "bytes": nbytes}
+                  "bytes": nbytes, "e2e_ms": e2e_ms,
+                  "h2d_bytes": sum(t.numel() * t.element_size() for t in host.values())}
             if orc is not None:
                 pt["parity_sample"] = check_relocate_sample(
                     dict(wl=wl, L=L, src=src, dst=dst, cfg=cfg), orc, n_rows=300, seed=7 + j)
@@ -1790,6 +1932,7 @@ def run_sweep_mla(args, rank, world, local):
     tot_ms = sum(p["ms"] for p in reloc)
     tot_bytes = sum(p["bytes"] for p in reloc)
     tot_kms = sum(p["kernel_ms"] for p in reloc)
+    tot_e2e_ms = sum(p["e2e_ms"] for p in reloc)
     achieved = tot_bytes / (tot_kms * 1e-3) / 1e9
     return {
         "metric": "relocated KV tokens/s (all layers)",
@@ -1801,13 +1944,25 @@ def run_sweep_mla(args, rank, world, local):
                                "relocation, chunk lengths x delta; splice with Delta = delta "
                                f"on one {n}-token sequence; standalone rank-{m} patch",
                    "value_is": "relocated tokens over all points / relocation time over all points",
+                   "steps_per_point": K, "warmup_per_point": W,
+                   "relocate_frac_min_max": [min(p["frac"] for p in reloc),
+                                             max(p["frac"] for p in reloc)],
+                   "splice_frac_by_delta": {str(p["delta"]): round(p["frac"], 3) for p in splice},
+                   "patch_frac_by_chunk_len": {str(p["chunk_len"]): round(p["frac"], 3)
+                                               for p in patch},
                    "relocate": reloc, "splice": splice, "patch": patch,
                    "l2": "relocation and patch move >= 4 GB per call; splice points say"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
                      "kernel": "relocate_kernel<MLA> over all sweep points",
-                     "kernel_ms": tot_kms / len(reloc)},
-        "e2e": None, "clocks": clk, "gpu_launches": launches,
+                     "kernel_ms": tot_kms / len(reloc),
+                     "algorithmic_bytes_per_launch": tot_bytes / len(reloc)},
+        "e2e": {"value": tot_tok * world / (tot_e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": sum(p["h2d_bytes"] for p in reloc) / len(reloc),
+                "d2h_bytes_per_step": 4,
+                "copies": "per relocation call: its index arrays from pinned host memory and "
+                          "the status word back"},
+        "clocks": clk, "gpu_launches": launches,
     }
 
 
@@ -2081,17 +2236,29 @@ WORKLOADS = {"relocate-mla": run_relocate_mla, "splice-mla-128k": run_splice_mla
              "relocate-mla-patch": run_relocate_mla_patch, "sweep-mla": run_sweep_mla,
              "splice-mla-128k-composed": run_splice_mla_128k_composed,
              "splice-mla-128k-remap": run_splice_mla_128k_remap,
+             "splice-mla-128k-remap-split":
+                 lambda a, r, w, l: run_splice_mla_128k_remap(a, r, w, l, split=True),
              "window-gqa": run_window_gqa, "cdc-tokens": run_cdc_tokens,
              "families": run_families}
+
+
+# The configured workloads, one JSON line each, the headline (the Irminsul
+# MLA relocation) last: the 4096-token splice, the 128K-context splice, the
+# Kamera GQA relocation with its fused rank-16 patch, the MLA sweep.
+DEFAULT_SEQUENCE = ("splice-mla-4k", "splice-mla-128k", "relocate-gqa-patch", "sweep-mla",
+                    "relocate-mla")
+SWEEP_MAX_STEPS = 10   # per sweep point in the default sequence (41 points)
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="relocate-mla")
+    ap.add_argument("--workload", choices=["default"] + sorted(WORKLOADS), default="default",
+                    help="default: every configured workload, one line each, the headline "
+                         "relocation last")
     ap.add_argument("--check", action="store_true", help="sampled parity vs the oracle")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true",
@@ -2110,15 +2277,33 @@ def main(argv=None):
     import position_independent_mla_gb300 as kv
 
     kv.load()  # raises if the CUDA library is missing: there is no fallback
+    names = DEFAULT_SEQUENCE if args.workload == "default" else (args.workload,)
+    cores = None
+    if rank == 0 and not args.no_cpu_baseline and any(n in CPU_SAMPLES for n in names):
+        cores = OracleCores()   # spawned processes, one per host core
     torch.cuda.set_device(local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
-    out = WORKLOADS[args.workload](args, rank, world, local)
-    if args.small and isinstance(out.get("roofline"), dict):
-        # the recorded DRAM traffic is that of the full workload
-        out["roofline"]["traffic"] = None
-    if rank == 0:
-        print(json.dumps(add_nominal(out)), flush=True)
+    try:
+        for name in names:
+            wargs = args
+            if name == "sweep-mla" and len(names) > 1:
+                wargs = argparse.Namespace(**dict(vars(args), steps=min(args.steps,
+                                                                       SWEEP_MAX_STEPS)))
+            out = WORKLOADS[name](wargs, rank, world, local)
+            gc.collect()
+            torch.cuda.empty_cache()   # the next workload gets the whole HBM
+            if args.small and isinstance(out.get("roofline"), dict):
+                # the recorded DRAM traffic is that of the full workload
+                out["roofline"]["traffic"] = None
+            if cores is not None and name in CPU_SAMPLES:
+                out["cpu_baseline"] = cpu_baseline(name, out["unit"], cores)
+            if rank == 0:
+                print(json.dumps(add_nominal(out)), flush=True)
+            barrier(world)
+    finally:
+        if cores is not None:
+            cores.close()
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0

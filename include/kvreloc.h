@@ -78,7 +78,11 @@ typedef enum {
     KV_ERR_WORKSPACE = 4,    /* workspace NULL, misaligned or smaller than needed */
     KV_ERR_TIMEOUT = 5,      /* (device) a bounded inter-block wait ran out */
     KV_ERR_CUDA = 6,         /* a CUDA runtime call failed */
-    KV_ERR_UNSUPPORTED = 7   /* a layout the kernels do not handle */
+    KV_ERR_UNSUPPORTED = 7,  /* a layout the kernels do not handle */
+    KV_ERR_OVERLAP = 8       /* (device, debug checks on) kv_relocate: a destination slot is
+                                also a source slot of the call in the same pool; kv_splice,
+                                kv_splice_composed: a block id appears twice among the
+                                block-table entries the call uses.  Nothing is stored. */
 } kv_status;
 
 /* Leyline directive modes (Leyline §2.1). */
@@ -124,9 +128,13 @@ typedef struct {
  * channels:
  *   d_u_chunk_tok[c]  U row of chunk c's first token (its tokens follow it),
  *   d_v_chunk[c]      V slot of chunk c;
- * the caller keeps every mapped row and slot inside the factor arrays.  An
- * MLA patch over the 576-wide row is one factor pair: u[0] = u[1],
- * v[1] = v[0] + 512*v_col_stride. */
+ * u_rows[ch] and v_slots[ch], when nonzero, are the extents of channel ch's
+ * factor arrays (U rows per layer, V slots per layer): a token whose U row
+ * (mapped or in call order) or a chunk whose V slot falls outside them is
+ * skipped and sets KV_ERR_OUT_OF_RANGE in the device status, like an index
+ * outside a pool.  0 leaves that extent unchecked (the caller then keeps every
+ * row and slot inside the arrays).  An MLA patch over the 576-wide row is one
+ * factor pair: u[0] = u[1], v[1] = v[0] + 512*v_col_stride. */
 typedef struct {
     int32_t rank; /* m: 4..64, a multiple of 4 */
     const float *u[2];
@@ -138,6 +146,8 @@ typedef struct {
     int64_t v_col_stride[2];
     const int64_t *d_u_chunk_tok; /* NULL: the call's token order */
     const int32_t *d_v_chunk;     /* NULL: the call's chunk order */
+    int64_t u_rows[2];            /* U rows per layer; 0 = unchecked */
+    int64_t v_slots[2];           /* V slots per layer; 0 = unchecked */
 } kv_patch_desc;
 
 /* Bytes of device workspace needed by any call on `pool` that moves at most
@@ -157,7 +167,9 @@ size_t kv_workspace_size(const kv_pool_desc *pool, int64_t max_rows, int32_t max
  * rotary head is turned by R(d_delta[c]).  `patch` (NULL = none) adds the
  * rank-m patch before the single rounding.
  * src and dst may be the same pool when no destination slot is also a source
- * slot (the call is not in place; overlapping slots give undefined rows).
+ * slot: the call is not in place, and overlapping slots give undefined rows
+ * unless the debug checks are on (kv_set_debug_checks), which then report
+ * KV_ERR_OVERLAP and store nothing.
  * Shapes (num_layers, copy_dim, rot_heads, rot_head_dim, rope_base) of src
  * and dst must match. */
 kv_status kv_relocate(const kv_pool_desc *src, const kv_pool_desc *dst, int32_t num_chunks,
@@ -182,7 +194,8 @@ kv_status kv_relocate(const kv_pool_desc *src, const kv_pool_desc *dst, int32_t 
  * h_seq_lens[q] becomes seq_len + Δ.  Slots at or beyond the new length keep
  * whatever they held.  Needs ceil(max(seq_len, seq_len+Δ)/block_size) <=
  * max_blocks (else KV_ERR_CAPACITY); the caller owns the blocks of every
- * entry used, distinct across the whole call.  The in-place shift is
+ * entry used, distinct across the whole call (checked, with KV_ERR_OVERLAP
+ * and nothing stored, when the debug checks are on).  The in-place shift is
  * overlap-safe for Δ of either sign.
  * FORGET: moves nothing and sets h_seq_lens[q] = s_start (the caller
  * re-prefills from there); no device work.
@@ -292,8 +305,12 @@ kv_status kv_patch(const kv_pool_desc *pool, int32_t num_chunks, int64_t total_t
  *    each call clears its status word first.  Calls that overlap on the GPU
  *    (different streams, not ordered) race on the array: order them.
  *  - h_device_status: when non-NULL the call waits for `stream` and stores
- *    the device status (KV_OK or KV_ERR_OUT_OF_RANGE) there; when NULL the
- *    call stays asynchronous and device-side errors are not reported.
+ *    the device status (KV_OK, KV_ERR_OUT_OF_RANGE, or KV_ERR_OVERLAP with
+ *    the debug checks on) there; when NULL the call stays asynchronous and
+ *    device-side errors are not reported.
+ *  - With the debug checks on (kv_set_debug_checks) and src, dst the same
+ *    pool, the overlap bitmap (one bit per slot) must also fit in the array,
+ *    else the call is rejected with KV_ERR_WORKSPACE.
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.
  * Arguments otherwise as kv_relocate. */
 kv_status kv_relocate_noalloc(const kv_pool_desc *src, const kv_pool_desc *dst,
@@ -305,7 +322,8 @@ kv_status kv_relocate_noalloc(const kv_pool_desc *src, const kv_pool_desc *dst,
                               int32_t *h_device_status, kv_stream_t stream);
 
 /* Wait for `stream`, then return the device status of the last call that
- * used this workspace (KV_OK, KV_ERR_OUT_OF_RANGE or KV_ERR_TIMEOUT), or
+ * used this workspace (KV_OK, KV_ERR_OUT_OF_RANGE, KV_ERR_CAPACITY from
+ * kv_cdc, KV_ERR_TIMEOUT, or KV_ERR_OVERLAP with the debug checks on), or
  * KV_ERR_CUDA if the synchronisation or the read failed. */
 kv_status kv_get_device_status(const void *d_workspace, kv_stream_t stream);
 
@@ -359,9 +377,42 @@ kv_status kv_fingerprint(int64_t num_ranges, const int64_t *d_start, const int64
                          uint64_t *d_fingerprint, void *d_workspace, size_t workspace_bytes,
                          kv_stream_t stream);
 
+/* Debug checks of the caller contracts that the in-place kernels rely on
+ * (process-wide; off by default).  When on:
+ *  - kv_relocate (and kv_relocate_noalloc) on a source and destination that
+ *    are the same pool (the same copy_base or the same rot_base) first marks
+ *    every source slot in a bitmap, then tests every destination slot against
+ *    it: a destination slot that is also a source slot of the call would be
+ *    read and written by different blocks in no fixed order (Irminsul §2.2:
+ *    the relocation gathers stored rows into new slots);
+ *  - kv_splice and kv_splice_composed mark every block-table entry the call
+ *    uses (ceil(max(old length, new length) / block_size) per sequence): a
+ *    block id that appears twice would make two logical positions share a
+ *    slot, and the in-place shift (Leyline §2.1-§2.3) would race on it.
+ * Either finding sets KV_ERR_OVERLAP in the device status, and the call's
+ * row-moving kernels then store nothing (the pools and block tables stay bit
+ * for bit as they were).  Cost when on: the workspace grows by one bit per
+ * slot of the destination pool, rounded up to 256 bytes (kv_workspace_size
+ * and kv_splice_composed_workspace_size always include it), plus one memset
+ * of that bitmap and one or two scan kernels over the call's index arrays (a
+ * few bytes per token or block-table entry, against the kilobytes per token
+ * that the rows move).  Cost when off: none -- the scans are not launched and
+ * no kernel reads anything more. */
+void kv_set_debug_checks(int32_t on);
+
 /* Upper bound, in nanoseconds, of every inter-block wait inside kv_splice
  * (default 2e9).  Values <= 0 restore the default.  Process-wide. */
 void kv_set_wait_limit_ns(int64_t limit_ns);
+
+/* Test hook for the failure path of the in-place splices (process-wide; -1,
+ * the default, turns it off).  The tile of each kv_splice / kv_splice_composed
+ * launch that draws ticket `ticket` does not publish that it has read its
+ * rows; the tiles whose destination overlaps those rows then wait in vain
+ * until the wait limit, record KV_ERR_TIMEOUT, skip their stores and keep
+ * publishing, so the launch still finishes.  Lets a test run the kernels' own
+ * timeout branch without faulting or hanging a GPU (give it a short
+ * kv_set_wait_limit_ns). */
+void kv_set_splice_skip_publish(int64_t ticket);
 
 /* Run the bounded wait used by kv_splice on a workspace flag that nothing
  * sets, with the given limit; the device status afterwards is

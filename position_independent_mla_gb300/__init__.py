@@ -23,6 +23,7 @@ from . import build as _build
 
 KV_OK, KV_ERR_INVALID_ARG, KV_ERR_OUT_OF_RANGE, KV_ERR_CAPACITY = 0, 1, 2, 3
 KV_ERR_WORKSPACE, KV_ERR_TIMEOUT, KV_ERR_CUDA, KV_ERR_UNSUPPORTED = 4, 5, 6, 7
+KV_ERR_OVERLAP = 8
 KV_AMORTIZE, KV_FORGET, KV_AMORTIZE_REMAP = 0, 1, 2
 
 LIB_PATH = _build.LIB
@@ -65,6 +66,8 @@ class kv_patch_desc(C.Structure):
         ("v_col_stride", C.c_int64 * 2),
         ("d_u_chunk_tok", C.c_void_p),
         ("d_v_chunk", C.c_void_p),
+        ("u_rows", C.c_int64 * 2),
+        ("v_slots", C.c_int64 * 2),
     ]
 
 
@@ -107,6 +110,8 @@ def load(build_if_missing: bool = False) -> C.CDLL:
                                           C.POINTER(i64), C.POINTER(i32)]),
         "kv_get_device_status": (i32, [vp, vp]),
         "kv_set_wait_limit_ns": (None, [i64]),
+        "kv_set_debug_checks": (None, [i32]),
+        "kv_set_splice_skip_publish": (None, [i64]),
         "kv_check_wait_timeout": (i32, [vp, sz, i64, vp]),
         "kv_last_launch_count": (i32, []),
         "kv_set_kernel_events": (None, [vp, vp]),
@@ -176,13 +181,16 @@ def pool_desc(copy: torch.Tensor, rot: torch.Tensor, block_size: int, rot_heads:
 
 def patch_desc(rank: int, u: Sequence[Optional[torch.Tensor]],
                v: Sequence[Optional[torch.Tensor]], u_chunk_tok: Optional[torch.Tensor] = None,
-               v_chunk: Optional[torch.Tensor] = None) -> kv_patch_desc:
+               v_chunk: Optional[torch.Tensor] = None,
+               check_extents: bool = True) -> kv_patch_desc:
     """Factors per channel (0 = verbatim part, 1 = rotated part): ``u[ch]``
     fp32 (L, tokens, rank), ``v[ch]`` fp32 (L, chunks, columns, rank), any
     strides with a unit last stride; None = channel not patched.  Optional
     device maps into factors kept per canonical chunk: ``u_chunk_tok`` int64
     (chunks,) U row of each chunk's first token, ``v_chunk`` int32 (chunks,)
-    V slot of each chunk."""
+    V slot of each chunk.  ``check_extents``: pass the factor arrays' row and
+    slot counts, so a token or chunk addressing outside them is skipped and
+    reported (KV_ERR_OUT_OF_RANGE) instead of read out of bounds."""
     d = kv_patch_desc()
     d.rank = rank
     # keep the factors and maps alive as long as the descriptor
@@ -206,6 +214,9 @@ def patch_desc(rank: int, u: Sequence[Optional[torch.Tensor]],
         d.v_layer_stride[ch] = vv.stride(0)
         d.v_chunk_stride[ch] = vv.stride(1)
         d.v_col_stride[ch] = vv.stride(2)
+        if check_extents:
+            d.u_rows[ch] = uu.shape[1]
+            d.v_slots[ch] = vv.shape[1]
     return d
 
 
@@ -361,6 +372,18 @@ def kv_get_device_status(ws: torch.Tensor, stream=None) -> int:
 
 def kv_set_wait_limit_ns(limit_ns: int) -> None:
     load().kv_set_wait_limit_ns(int(limit_ns))
+
+
+def kv_set_debug_checks(on: bool) -> None:
+    """Process-wide: check the overlap / distinct-block contracts on the device
+    before every relocation and splice (KV_ERR_OVERLAP, nothing stored)."""
+    load().kv_set_debug_checks(1 if on else 0)
+
+
+def kv_set_splice_skip_publish(ticket: int) -> None:
+    """Test hook: the splice tile drawing ``ticket`` does not publish its reads
+    (its dependants time out); -1 turns it off."""
+    load().kv_set_splice_skip_publish(int(ticket))
 
 
 def kv_check_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> int:

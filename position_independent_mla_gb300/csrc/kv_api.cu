@@ -20,6 +20,8 @@ namespace {
 
 constexpr int64_t kDefaultWaitLimitNs = 2000000000ll;
 std::atomic<int64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
+std::atomic<int32_t> g_debug_checks{0};   // kv_set_debug_checks
+std::atomic<int64_t> g_skip_publish{-1};  // kv_set_splice_skip_publish (test hook)
 thread_local int32_t t_launches = 0;
 thread_local cudaEvent_t t_ev_start = nullptr, t_ev_stop = nullptr;
 
@@ -102,6 +104,49 @@ size_t table_bytes(const kv_pool_desc *p, int64_t units)
     return align256((size_t)units * (size_t)(p->rot_head_dim / 2) * sizeof(float4));
 }
 
+// Debug checks: a bitmap of `bits` bits, and the per-sequence entry counts of
+// a splice.
+size_t bitmap_bytes(int64_t bits) { return align256((size_t)((bits + 31) / 32) * 4u); }
+
+size_t debug_bytes(const kv_pool_desc *p, int64_t seqs)
+{
+    return bitmap_bytes(p->num_slots) + align256((size_t)std::max<int64_t>(seqs, 0) * 4u);
+}
+
+// Source and destination share their slots (a relocation inside one pool).
+bool same_pool(const kv_pool_desc *a, const kv_pool_desc *b)
+{
+    return a->copy_base == b->copy_base || a->rot_base == b->rot_base;
+}
+
+// Debug check of a splice's block-table entries: `used[q]` entries of row q
+// must name distinct blocks.  Copies the counts into the workspace at `at`
+// (pageable host memory: the call returns once the driver holds its copy)
+// and launches the scan; returns the gate for the row-moving kernels.
+cudaError_t launch_dup_check(const kv_pool_desc *pool, const int32_t *d_block_tables,
+                             int32_t max_blocks, const std::vector<int32_t> &used, char *at,
+                             uint32_t *status, cudaStream_t stream)
+{
+    const int64_t nb = pool->num_slots / pool->block_size;
+    uint32_t *bm = reinterpret_cast<uint32_t *>(at);
+    int32_t *d_used = reinterpret_cast<int32_t *>(at + bitmap_bytes(pool->num_slots));
+    cudaError_t e = cudaMemsetAsync(bm, 0, bitmap_bytes(nb), stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(d_used, used.data(), used.size() * sizeof(int32_t),
+                            cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess)
+        return e;
+    DupBlockParams dp{};
+    dp.block_tables = d_block_tables;
+    dp.used = d_used;
+    dp.rows = (int32_t)used.size();
+    dp.max_blocks = max_blocks;
+    dp.num_blocks = nb;
+    dp.bitmap = bm;
+    dp.status = status;
+    return launch_dup_block_check(dp, stream);
+}
+
 // Factor checks; fills `pv` and tells whether any channel is patched.
 kv_status patch_view(const kv_patch_desc *d, PatchView *pv, bool *any)
 {
@@ -133,6 +178,10 @@ kv_status patch_view(const kv_patch_desc *d, PatchView *pv, bool *any)
         pv->v_ls[ch] = d->v_layer_stride[ch];
         pv->v_cs[ch] = d->v_chunk_stride[ch];
         pv->v_cols[ch] = d->v_col_stride[ch];
+        if (d->u_rows[ch] < 0 || d->v_slots[ch] < 0)
+            return KV_ERR_INVALID_ARG;
+        pv->u_rows[ch] = d->u_rows[ch];
+        pv->v_slots[ch] = d->v_slots[ch];
         *any = true;
     }
     return KV_OK;
@@ -191,13 +240,39 @@ kv_status relocate_impl(const kv_pool_desc *src, const kv_pool_desc *dst, int32_
     if (in_place && !patched)
         return KV_ERR_INVALID_ARG;
     const size_t need = kHeaderBytes + (in_place ? 0 : table_bytes(src, num_chunks));
-    if ((st = ws_ok(ws, ws_bytes, need)) != KV_OK)
+    // debug check: a relocation inside one pool must not write a slot it reads
+    const bool check = !in_place && g_debug_checks.load() != 0 && same_pool(src, dst);
+    const size_t check_bytes = check ? bitmap_bytes(dst->num_slots) : 0;
+    if ((st = ws_ok(ws, ws_bytes, need + check_bytes)) != KV_OK)
         return st;
 
     char *w = static_cast<char *>(ws);
     KV_CUDA(cudaMemsetAsync(w, 0, kHeaderBytes, stream));
     if (total_tokens == 0)
         return KV_OK;
+    const uint32_t *gate = nullptr;
+    if (check) {
+        uint32_t *bm = reinterpret_cast<uint32_t *>(w + need);
+        KV_CUDA(cudaMemsetAsync(bm, 0, check_bytes, stream));
+        OverlapParams op{};
+        op.tok_off = tok_off;
+        op.src_slots = src_slots;
+        op.chunk_req = chunk_req;
+        op.chunk_dst_pos = chunk_dst_pos;
+        op.block_tables = block_tables;
+        op.num_chunks = num_chunks;
+        op.num_reqs = num_reqs;
+        op.max_blocks = max_blocks;
+        op.block = dst->block_size;
+        op.total_tokens = total_tokens;
+        op.num_slots = dst->num_slots;
+        op.num_blocks = dst->num_slots / dst->block_size;
+        op.bitmap = bm;
+        op.status = reinterpret_cast<uint32_t *>(w);
+        KV_CUDA(launch_overlap_check(op, stream));
+        t_launches += 2;
+        gate = reinterpret_cast<uint32_t *>(w);
+    }
     float4 *table = reinterpret_cast<float4 *>(w + kHeaderBytes);
     if (!in_place) {
         TableParams tp{};
@@ -228,6 +303,7 @@ kv_status relocate_impl(const kv_pool_desc *src, const kv_pool_desc *dst, int32_
     rp.patched = patched ? 1 : 0;
     rp.in_place = in_place ? 1 : 0;
     rp.status = reinterpret_cast<uint32_t *>(w);
+    rp.gate = gate;
     KV_CUDA(mark(t_ev_start, stream));
     if (patch_tc_supported(rp, kind)) {
         KV_CUDA(launch_patch_tc(rp, kind, stream));
@@ -456,7 +532,9 @@ size_t kv_workspace_size(const kv_pool_desc *pool, int64_t max_rows, int32_t max
     const int64_t T = std::min(tile_rows(kind), inplace_tile_rows(kind));
     const int64_t units = std::max<int64_t>(max_units, 1);
     const int64_t flags = (int64_t)pool->num_layers * ((max_rows + T - 1) / T + units);
-    return (size_t)kHeaderBytes + table_bytes(pool, units) + align256((size_t)flags * 4u);
+    // the last part serves the debug checks (kv_set_debug_checks)
+    return (size_t)kHeaderBytes + table_bytes(pool, units) + align256((size_t)flags * 4u) +
+           debug_bytes(pool, units);
 }
 
 kv_status kv_relocate(const kv_pool_desc *src, const kv_pool_desc *dst, int32_t num_chunks,
@@ -540,7 +618,6 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
 
     // plan: launches of up to kMaxSeqsPerLaunch sequences each
     const int T = inplace_tile_rows(kind);
-    const int L = pool->num_layers;
     std::vector<SpliceParams> plans;
     int64_t stub_base = 0, max_flags = 0;
     for (int q0 = 0; q0 < num_seqs; q0 += kMaxSeqsPerLaunch) {
@@ -572,7 +649,9 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
     }
     const size_t tbytes = table_bytes(pool, std::min(num_seqs, kMaxSeqsPerLaunch));
     const size_t need = kHeaderBytes + tbytes + align256((size_t)max_flags * 4u);
-    kv_status st = ws_ok(d_workspace, workspace_bytes, need);
+    const bool check = g_debug_checks.load() != 0;
+    kv_status st =
+        ws_ok(d_workspace, workspace_bytes, need + (check ? debug_bytes(pool, num_seqs) : 0));
     if (st != KV_OK)
         return st;
 
@@ -582,7 +661,22 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
     float4 *table = reinterpret_cast<float4 *>(w + kHeaderBytes);
     uint32_t *flags = reinterpret_cast<uint32_t *>(w + kHeaderBytes + tbytes);
     KV_CUDA(cudaMemsetAsync(w, 0, kHeaderBytes, stream));
+    const uint32_t *gate = nullptr;
+    if (check) {
+        // the entries each sequence uses, before and after its directive
+        std::vector<int32_t> used((size_t)num_seqs);
+        for (int q = 0; q < num_seqs; ++q) {
+            const int64_t new_len =
+                (int64_t)h_seq_lens[q] + h_stub_len[q] - (h_s_end[q] - h_s_start[q]);
+            used[q] = (int32_t)((std::max<int64_t>(h_seq_lens[q], new_len) + B - 1) / B);
+        }
+        KV_CUDA(launch_dup_check(pool, d_block_tables, max_blocks, used, w + need, status,
+                                 stream));
+        ++t_launches;
+        gate = status;
+    }
     const int64_t limit = g_wait_limit_ns.load();
+    const int64_t skip = g_skip_publish.load();
     bool marked = false;
     for (SpliceParams &sp : plans) {
         if (sp.total_tickets == 0)
@@ -615,6 +709,8 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
         sp.ticket = ticket;
         sp.flags = flags;
         sp.wait_limit_ns = limit;
+        sp.skip_publish = skip;
+        sp.gate = gate;
         if (!marked) {
             KV_CUDA(mark(t_ev_start, stream));
             marked = true;
@@ -674,6 +770,7 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
         rp.total_stub = total_stub;
         rp.table = table;
         rp.status = status;
+        rp.gate = gate;
         if (!marked) {
             KV_CUDA(mark(t_ev_start, stream));
             marked = true;
@@ -703,7 +800,8 @@ size_t kv_splice_composed_workspace_size(const kv_pool_desc *pool, int32_t num_s
     if (plan_composed(kind, num_seqs, num_dirs, -1, h_seq_lens, h_s_start, h_s_end, h_stub_len,
                       plan) != KV_OK)
         return 0;
-    return composed_bytes(pool, plan);
+    // the last part serves the debug checks (kv_set_debug_checks)
+    return composed_bytes(pool, plan) + debug_bytes(pool, num_seqs);
 }
 
 kv_status kv_splice_composed(const kv_pool_desc *pool, int32_t num_seqs, int32_t num_dirs,
@@ -735,7 +833,10 @@ kv_status kv_splice_composed(const kv_pool_desc *pool, int32_t num_seqs, int32_t
     if (plan.total_stub > 0 && (!d_stub_copy || !d_stub_rot || !aligned16(d_stub_copy) ||
                                 !aligned16(d_stub_rot)))
         return KV_ERR_INVALID_ARG;
-    if ((st = ws_ok(d_workspace, workspace_bytes, composed_bytes(pool, plan))) != KV_OK)
+    const size_t need = composed_bytes(pool, plan);
+    const bool check = g_debug_checks.load() != 0;
+    if ((st = ws_ok(d_workspace, workspace_bytes,
+                    need + (check ? debug_bytes(pool, num_seqs) : 0))) != KV_OK)
         return st;
 
     char *w = static_cast<char *>(d_workspace);
@@ -748,6 +849,17 @@ kv_status kv_splice_composed(const kv_pool_desc *pool, int32_t num_seqs, int32_t
     uint32_t *flags = reinterpret_cast<uint32_t *>(
         w + kHeaderBytes + tbytes + tiles_bytes + align256(plan.deltas.size() * sizeof(int32_t)));
     KV_CUDA(cudaMemsetAsync(w, 0, kHeaderBytes, stream));
+    const uint32_t *gate = nullptr;
+    if (check) {
+        const int64_t B = pool->block_size;
+        std::vector<int32_t> used((size_t)num_seqs);
+        for (int32_t q = 0; q < num_seqs; ++q)
+            used[q] = (int32_t)((std::max<int64_t>(h_seq_lens[q], plan.final_len[q]) + B - 1) / B);
+        KV_CUDA(launch_dup_check(pool, d_block_tables, max_blocks, used, w + need, status,
+                                 stream));
+        ++t_launches;
+        gate = status;
+    }
     if (!plan.tiles.empty()) {
         // the plan is copied from pageable host memory: the call returns once
         // the driver holds its own copy, so the vectors may go out of scope
@@ -783,6 +895,8 @@ kv_status kv_splice_composed(const kv_pool_desc *pool, int32_t num_seqs, int32_t
         cp.flags = flags;
         cp.num_tiles = (int64_t)plan.tiles.size();
         cp.wait_limit_ns = g_wait_limit_ns.load();
+        cp.skip_publish = g_skip_publish.load();
+        cp.gate = gate;
         KV_CUDA(mark(t_ev_start, stream));
         KV_CUDA(launch_splice_composed(cp, kind, stream));
         KV_CUDA(mark(t_ev_stop, stream));
@@ -944,6 +1058,10 @@ void kv_set_wait_limit_ns(int64_t limit_ns)
     g_wait_limit_ns.store(limit_ns > 0 ? limit_ns : kDefaultWaitLimitNs);
 }
 
+void kv_set_debug_checks(int32_t on) { g_debug_checks.store(on != 0 ? 1 : 0); }
+
+void kv_set_splice_skip_publish(int64_t ticket) { g_skip_publish.store(ticket >= 0 ? ticket : -1); }
+
 kv_status kv_check_wait_timeout(void *d_workspace, size_t workspace_bytes, int64_t limit_ns,
                                 kv_stream_t stream_)
 {
@@ -988,11 +1106,13 @@ const char *kv_status_string(kv_status s)
         return "CUDA runtime error";
     case KV_ERR_UNSUPPORTED:
         return "unsupported layout";
+    case KV_ERR_OVERLAP:
+        return "overlapping slots or duplicate blocks (debug check)";
     }
     return "unknown status";
 }
 
-int32_t kv_version(void) { return 100; }
+int32_t kv_version(void) { return 200; }
 
 } // extern "C"
 

@@ -17,7 +17,21 @@ constexpr int kTileGqa4 = 32;         // rows per tile for 4 x 128 GQA rows
 constexpr int kTileMha = 4;           // rows per tile for 32 x 128 MHA rows
 
 // Device status codes (same values as kv_status).
-enum : uint32_t { kStatusOk = 0, kStatusOutOfRange = 2, kStatusCapacity = 3, kStatusTimeout = 5 };
+enum : uint32_t {
+    kStatusOk = 0,
+    kStatusOutOfRange = 2,
+    kStatusCapacity = 3,
+    kStatusTimeout = 5,
+    kStatusOverlap = 8
+};
+
+// Row-moving kernels of a call made with the debug checks on read the
+// status word first (`gate`; nullptr when the checks are off) and store
+// nothing when a check found an overlap.
+__device__ __forceinline__ bool gate_closed(const uint32_t *gate)
+{
+    return gate != nullptr && *reinterpret_cast<const volatile uint32_t *>(gate) == kStatusOverlap;
+}
 
 // A pool as the kernels see it: byte addresses and byte strides.
 struct PoolView {
@@ -40,7 +54,25 @@ struct PatchView {
     int64_t v_ls[2], v_cs[2], v_cols[2];
     const int64_t *u_chunk_tok; // per chunk: U row of its first token (nullptr: call order)
     const int32_t *v_chunk;     // per chunk: V slot (nullptr: call order)
+    int64_t u_rows[2];          // extents of the factor arrays (0: unchecked)
+    int64_t v_slots[2];
 };
+
+// True when U row `urow` and V slot `vslot` lie inside the extents of every
+// patched channel (an extent of 0 is not checked).
+__host__ __device__ __forceinline__ bool patch_rows_ok(const PatchView &pv, int64_t urow,
+                                                       int64_t vslot)
+{
+    for (int ch = 0; ch < 2; ++ch) {
+        if (pv.u[ch] == nullptr)
+            continue;
+        if (pv.u_rows[ch] > 0 && (urow < 0 || urow >= pv.u_rows[ch]))
+            return false;
+        if (pv.v_slots[ch] > 0 && (vslot < 0 || vslot >= pv.v_slots[ch]))
+            return false;
+    }
+    return true;
+}
 
 // kv_relocate (in_place = 0) and kv_patch (in_place = 1: rows are read from
 // and written back to the destination slots, without rotation).
@@ -60,6 +92,7 @@ struct RelocParams {
     int32_t patched;
     int32_t in_place;
     uint32_t *status;
+    const uint32_t *gate; // debug checks: the status word (else nullptr)
 };
 
 // Host-side plan of one sequence of a splice launch.
@@ -87,6 +120,8 @@ struct SpliceParams {
     uint32_t *flags;
     int64_t total_tickets;
     int64_t wait_limit_ns;
+    int64_t skip_publish; // test hook: this ticket does not publish its reads (-1: none)
+    const uint32_t *gate;
     int32_t num_seqs;
     SpliceSeq seq[kMaxSeqsPerLaunch];
 };
@@ -121,6 +156,8 @@ struct ComposedParams {
     uint32_t *flags; // [num_tiles] (layer, warp) read counters
     int64_t num_tiles;
     int64_t wait_limit_ns;
+    int64_t skip_publish; // test hook (-1: none)
+    const uint32_t *gate;
 };
 
 // Block-aligned splice by remapping (s_start, s_end, n_r multiples of the
@@ -145,9 +182,36 @@ struct RemapParams {
     int64_t total_stub;
     const float4 *table; // [num_seqs][head_dim/2]
     uint32_t *status;
+    const uint32_t *gate;
     int64_t total_tiles;
     int32_t num_seqs;
     RemapSeq seq[kMaxSeqsPerLaunch];
+};
+
+// Debug check of a relocation in one pool: mark the source slots, then test
+// the destination slots (bitmap of num_slots bits).
+struct OverlapParams {
+    const int32_t *tok_off;
+    const int32_t *src_slots;
+    const int32_t *chunk_req;
+    const int32_t *chunk_dst_pos;
+    const int32_t *block_tables;
+    int32_t num_chunks, num_reqs, max_blocks, block;
+    int64_t total_tokens;
+    int64_t num_slots;  // of the destination pool
+    int64_t num_blocks;
+    uint32_t *bitmap;
+    uint32_t *status;
+};
+
+// Debug check of a splice: every used block-table entry marked once.
+struct DupBlockParams {
+    const int32_t *block_tables;
+    const int32_t *used; // entries used per block-table row [rows]
+    int32_t rows, max_blocks;
+    int64_t num_blocks;
+    uint32_t *bitmap;
+    uint32_t *status;
 };
 
 struct TableParams {

@@ -30,13 +30,16 @@ cudaError_t launch_remap(const RemapParams &p, RowKind kind, cudaStream_t stream
 constexpr int32_t kMaxRemapBlocks = 48 * 1024; // block-table entries one commit block holds
 cudaError_t launch_wait_check(uint32_t *flag, uint32_t *status, int64_t limit_ns,
                               cudaStream_t stream);
+// Debug checks (kv_set_debug_checks): relocation overlap, duplicate blocks.
+cudaError_t launch_overlap_check(const OverlapParams &p, cudaStream_t stream);
+cudaError_t launch_dup_block_check(const DupBlockParams &p, cudaStream_t stream);
 // Content-defined chunking: flags, scan, emit (+ fingerprint) kernels.
 int64_t cdc_blocks(int64_t total_tokens);
 cudaError_t launch_cdc(const CdcParams &p, cudaStream_t stream);
 cudaError_t launch_fingerprint(const FingerprintParams &p, cudaStream_t stream);
 constexpr int kCdcLaunches = 3;
 
-// Rows per tile of each kind for the relocation and the composed splice.
+// Rows per tile of each kind for the relocation (launch_relocate).
 inline int tile_rows(RowKind kind)
 {
     switch (kind) {
@@ -53,13 +56,14 @@ inline int tile_rows(RowKind kind)
 }
 
 // Rows per tile of the in-place passes over multi-head rows (the ticketed
-// splice and the block-table remap): half the rows of the relocation's
-// tiles, at four blocks per SM.
+// splice, the composed splice and the block-table remap): half the rows of
+// the relocation's tiles, at four blocks per SM.
 constexpr int kInPlaceTileGqa = 8;
 constexpr int kInPlaceTileGqa4 = 16;
 constexpr int kInPlaceTileMha = 2;
 
-// Rows per tile of launch_splice and launch_remap.
+// Rows per tile of launch_splice, launch_splice_composed (and the host plan
+// of its tiles) and launch_remap; the kernels' G::T must equal it.
 inline int inplace_tile_rows(RowKind kind)
 {
     switch (kind) {

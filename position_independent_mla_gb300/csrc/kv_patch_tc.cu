@@ -230,6 +230,8 @@ __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaun
     __shared__ uint32_t s_tmem;
     __shared__ int32_t s_ok;
 
+    if (gate_closed(p.gate))
+        return; // a debug check found an overlap: store nothing
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int per_chunk = tl.nch * tl.slices;
     const int c = bx / per_chunk, l = blockIdx.y;
@@ -246,6 +248,15 @@ __device__ __forceinline__ void patch_tc_body(const RelocParams &p, const TcLaun
     const int64_t n = max((int64_t)0, (int64_t)p.tok_off[c + 1] - t0);
     // U row of the chunk's first token: call order, or the caller's map
     const int64_t u0 = p.patch.u_chunk_tok ? p.patch.u_chunk_tok[c] : t0;
+    if (patched) {
+        // the chunk's U rows and V slot must lie inside the stated extents
+        const int64_t vs = p.patch.v_chunk ? p.patch.v_chunk[c] : c;
+        if (n > 0 && !(patch_rows_ok(p.patch, u0, vs) && patch_rows_ok(p.patch, u0 + n - 1, vs))) {
+            if (tid == 0)
+                set_status(p.status, kStatusOutOfRange);
+            return; // block-uniform: nothing allocated yet
+        }
+    }
     const int32_t req = p.chunk_req[c];
     const bool req_ok = req >= 0 && req < p.num_reqs;
     const int32_t *bt = p.block_tables + (int64_t)(req_ok ? req : 0) * p.max_blocks;

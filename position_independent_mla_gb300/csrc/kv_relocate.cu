@@ -7,6 +7,8 @@
 // block handles T consecutive tokens of the call for all layers, so the
 // per-token index work (chunk search, block-table lookup) and the cos/sin
 // rows are set up once and reused for every layer.
+#include <algorithm>
+
 #include "kv_launch.h"
 #include "kv_tiles.cuh"
 
@@ -24,25 +26,30 @@ __device__ __forceinline__ double lead16(double x)
 
 __global__ void delta_table_kernel(const __grid_constant__ TableParams p)
 {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= p.units * p.half)
-        return;
-    const int u = i / p.half, j = i % p.half;
-    const int32_t delta = p.d_delta ? p.d_delta[u] : p.h_delta[u];
-    const double theta = pow(p.base, -2.0 * (double)j / (double)p.head_dim);
-    const double a = (double)delta * theta;
-    double s, c;
-    sincos(a, &s, &c);
-    const double c1 = lead16(c), s1 = lead16(s);
-    p.table[i] = make_float4((float)c1, (float)(c - c1), (float)s1, (float)(s - s1));
+    // 64-bit indices and a grid-stride loop: units * half may exceed 2^31
+    const int64_t n = (int64_t)p.units * p.half;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t u = i / p.half;
+        const int j = (int)(i % p.half);
+        const int32_t delta = p.d_delta ? p.d_delta[u] : p.h_delta[u];
+        const double theta = pow(p.base, -2.0 * (double)j / (double)p.head_dim);
+        const double a = (double)delta * theta;
+        double s, c;
+        sincos(a, &s, &c);
+        const double c1 = lead16(c), s1 = lead16(s);
+        p.table[i] = make_float4((float)c1, (float)(c - c1), (float)s1, (float)(s - s1));
+    }
 }
 
 cudaError_t launch_delta_table(const TableParams &p, cudaStream_t stream)
 {
-    const int n = p.units * p.half;
-    if (n == 0)
+    const int64_t n = (int64_t)p.units * p.half;
+    if (n <= 0)
         return cudaSuccess;
-    delta_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(p);
+    // at most 152 SMs x 16 blocks of 256 threads; larger tables loop
+    const int64_t blocks = std::min<int64_t>((n + 255) / 256, 152 * 16);
+    delta_table_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -61,6 +68,8 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const
     __shared__ int32_t s_ident[G::T];
     __shared__ float4 s_cs[G::T][G::kCsRow];
 
+    if (gate_closed(p.gate))
+        return; // a debug check found an overlap: store nothing
     const int tid = threadIdx.x;
     const int64_t tile0 = (int64_t)blockIdx.x * G::T;
 
@@ -107,11 +116,18 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) relocate_kernel(const
         s_dst[tid] = dst;
         // the patch's U row and V slot: call order, or the caller's maps
         const bool live = t < p.total_tokens;
-        s_tok[tid] = (live && p.patch.u_chunk_tok)
-                         ? p.patch.u_chunk_tok[c] + (t - p.tok_off[c])
-                         : t;
+        const int64_t urow = (live && p.patch.u_chunk_tok)
+                                 ? p.patch.u_chunk_tok[c] + (t - p.tok_off[c])
+                                 : t;
+        const int32_t vslot = (live && p.patch.v_chunk) ? p.patch.v_chunk[c] : c;
+        if (PATCH && src >= 0 && !patch_rows_ok(p.patch, urow, vslot)) {
+            // a factor row or slot outside the caller's stated extents
+            set_status(p.status, kStatusOutOfRange);
+            s_src[tid] = s_dst[tid] = -1;
+        }
+        s_tok[tid] = urow;
         s_chunk[tid] = c;
-        s_vslot[tid] = (live && p.patch.v_chunk) ? p.patch.v_chunk[c] : c;
+        s_vslot[tid] = vslot;
         s_ident[tid] = ident;
     }
     __syncthreads();

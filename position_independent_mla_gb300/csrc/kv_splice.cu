@@ -46,6 +46,8 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
     __shared__ float4 s_cs[G::kHalf];
     __shared__ uint32_t s_sink;
 
+    if (gate_closed(p.gate))
+        return; // a debug check found a duplicate block: every block leaves
     const int tid = threadIdx.x;
     if (tid == 0) {
         s_ticket = atomicAdd(p.ticket, 1u);
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
         // progress never waits on the tiles behind it (its source rows are
         // overwritten only by itself and by later tiles)
         __syncwarp();
-        if (shift && (tid & 31) == 0)
+        if (shift && (tid & 31) == 0 && t != p.skip_publish)
             red_release_add(p.flags + S.flag_base + k, 1u);
         const uint32_t want = ((uint32_t)l + 1u) * kWarps; // every warp has read layer l
         if (tid == 0 && !s_abort) {
@@ -219,6 +221,8 @@ splice_composed_kernel(const __grid_constant__ ComposedParams p)
     __shared__ float4 s_cs[G::kHalf];
     __shared__ uint32_t s_sink;
 
+    if (gate_closed(p.gate))
+        return; // a debug check found a duplicate block: every block leaves
     const int tid = threadIdx.x;
     if (tid == 0) {
         s_ticket = atomicAdd(p.ticket, 1u);
@@ -274,7 +278,7 @@ splice_composed_kernel(const __grid_constant__ ComposedParams p)
             s_sink = f;
         // this warp's share of layer l is read: publish before waiting
         __syncwarp();
-        if (!tile.stub && (tid & 31) == 0)
+        if (!tile.stub && (tid & 31) == 0 && t != p.skip_publish)
             red_release_add(p.flags + t, 1u);
         const uint32_t want = ((uint32_t)l + 1u) * kWarps;
         if (tid == 0 && !s_abort) {
@@ -358,6 +362,8 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(con
     __shared__ int32_t s_ident[G::T];
     __shared__ float4 s_cs[G::kHalf];
 
+    if (gate_closed(p.gate))
+        return;
     const int tid = threadIdx.x;
     const int64_t t = blockIdx.x;
     int q = 0;
@@ -443,6 +449,8 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(con
 __global__ void remap_commit_kernel(const __grid_constant__ RemapParams p)
 {
     extern __shared__ int32_t s_old[];
+    if (gate_closed(p.gate))
+        return; // the block-table rows stay as they were
     const RemapSeq &S = p.seq[blockIdx.x];
     int32_t *row = p.block_tables + (int64_t)S.bt_row * p.max_blocks;
     const int32_t B = p.pool.block;

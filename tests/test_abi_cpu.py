@@ -158,3 +158,45 @@ def test_misaligned_index_arrays_are_rejected(lib):
                      check=False) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_fingerprint(2, ok4, ok4, 10, bad4, 0, ok4, ws_t,
                              check=False) == kv.KV_ERR_INVALID_ARG
+
+
+def test_debug_checks_need_their_bitmap(lib):
+    """With the debug checks on, a relocation inside one pool and a splice need
+    the bitmap part of the workspace (one bit per slot); kv_workspace_size
+    always includes it.  Only rejections are exercised here: nothing reaches
+    the device."""
+    slots = 1 << 20
+    p = _fake_pool(slots=slots)
+    assert kv.kv_workspace_size(p, 1000, 4) >= slots // 8
+    assert kv.status_string(kv.KV_ERR_OVERLAP).startswith("overlapping")
+    ws = C.c_void_p(1 << 24)
+    a = C.c_void_p(256)
+    exact = 256 + 512            # header + cos/sin table of one 64-dim chunk
+    kv.kv_set_debug_checks(True)
+    try:
+        assert lib.kv_relocate(C.byref(p), C.byref(p), 1, 10, a, a, a, a, a, a, 1, 1, None, ws,
+                               exact, None) == kv.KV_ERR_WORKSPACE
+        i32 = lambda *v: torch.tensor(v, dtype=torch.int32)
+        lens = i32(100)
+        # header + table + three tiles' counters: enough without the checks
+        assert kv.kv_splice(p, 1, a, 4, lens, i32(10), i32(20), i32(0), None, None,
+                            kv.KV_AMORTIZE, torch.empty(0, dtype=torch.uint8), check=False) \
+            == kv.KV_ERR_WORKSPACE
+        assert lib.kv_splice(C.byref(p), 1, a, 4, lens.data_ptr(), i32(10).data_ptr(),
+                             i32(20).data_ptr(), i32(0).data_ptr(), None, None, kv.KV_AMORTIZE,
+                             ws, 256 + 512 + 256, None) == kv.KV_ERR_WORKSPACE
+        assert lens.tolist() == [100]
+    finally:
+        kv.kv_set_debug_checks(False)
+
+
+def test_patch_extents_are_validated_on_the_host(lib):
+    p = _fake_pool()
+    d = kv.kv_patch_desc()
+    d.rank = 8
+    d.u[0] = d.u[1] = 1 << 20
+    d.v[0] = d.v[1] = 1 << 21
+    d.u_rows[0] = -1
+    assert lib.kv_patch(C.byref(p), 1, 10, C.c_void_p(256), C.c_void_p(256), C.c_void_p(256),
+                        C.c_void_p(256), 1, 1, C.byref(d), C.c_void_p(1 << 24), 1 << 20,
+                        None) == kv.KV_ERR_INVALID_ARG

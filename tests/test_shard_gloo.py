@@ -61,10 +61,36 @@ def test_oracle_on_every_core_counts_every_unit():
 
     cores = bench.OracleCores(2)
     try:
-        ntok, dt = cores.run(16, 3)
+        ntok, dt, what = cores.run("relocate-mla", 16, 3)
     finally:
         cores.close()
-    assert ntok == 32 and dt > 0
+    assert ntok == 32 and dt > 0 and "16-token" in what
+
+
+@pytest.mark.parametrize("kind,n", [("relocate-mla", 16), ("sweep-mla", 1),
+                                    ("relocate-gqa-patch", 1), ("splice-mla-128k", 1024),
+                                    ("splice-mla-4k", 0)])
+def test_every_cpu_baseline_sample_runs_and_counts_its_units(kind, n):
+    """Each workload's oracle sample runs and reports the metric's units of
+    one call: tokens relocated, or rows moved by the splice (downstream rows
+    plus stub rows)."""
+    import bench
+
+    call, units, what = bench.oracle_sample(kind, n, 5)
+    call()
+    if kind == "splice-mla-4k":
+        assert units == 4096 - 2048 + 16
+    elif kind == "relocate-mla":
+        assert units == n
+    assert units > 0 and what
+
+
+def test_default_sequence_ends_with_the_headline():
+    import bench
+
+    assert bench.DEFAULT_SEQUENCE[-1] == "relocate-mla"
+    for name in bench.DEFAULT_SEQUENCE:
+        assert name in bench.WORKLOADS and name in bench.CPU_SAMPLES
 
 
 def test_reference_arm_prints_one_complete_line(capsys):

@@ -19,6 +19,11 @@ using namespace kvr;
 namespace {
 
 constexpr int64_t kDefaultWaitLimitNs = 2000000000ll;
+// Splice launches of at most this many tiles (a wave or two) form their
+// cos/sin rows inside the splice kernel instead of launching the δ-table
+// kernel: each block spends a few fp64 sincos on its prologue, which only
+// pays off while the launch is short.
+constexpr int64_t kInlineTableTiles = 1024;
 std::atomic<int64_t> g_wait_limit_ns{kDefaultWaitLimitNs};
 std::atomic<int32_t> g_debug_checks{0};   // kv_set_debug_checks
 std::atomic<int64_t> g_skip_publish{-1};  // kv_set_splice_skip_publish (test hook)
@@ -655,12 +660,22 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
     if (st != KV_OK)
         return st;
 
+    // workspace: header, the tiles' read counters, the δ-table (then the
+    // debug-check part); the header and the first launch's counters are
+    // cleared by one memset
     char *w = static_cast<char *>(d_workspace);
     uint32_t *status = reinterpret_cast<uint32_t *>(w);
     uint32_t *ticket = status + 1;
-    float4 *table = reinterpret_cast<float4 *>(w + kHeaderBytes);
-    uint32_t *flags = reinterpret_cast<uint32_t *>(w + kHeaderBytes + tbytes);
-    KV_CUDA(cudaMemsetAsync(w, 0, kHeaderBytes, stream));
+    uint32_t *flags = reinterpret_cast<uint32_t *>(w + kHeaderBytes);
+    float4 *table = reinterpret_cast<float4 *>(w + kHeaderBytes + align256((size_t)max_flags * 4u));
+    size_t first_flags = 0;
+    for (const SpliceParams &sp : plans)
+        if (sp.total_tickets > 0) {
+            for (int i = 0; i < sp.num_seqs; ++i)
+                first_flags += (size_t)sp.seq[i].n_shift;
+            break;
+        }
+    KV_CUDA(cudaMemsetAsync(w, 0, kHeaderBytes + first_flags * 4u, stream));
     const uint32_t *gate = nullptr;
     if (check) {
         // the entries each sequence uses, before and after its directive
@@ -677,27 +692,37 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
     }
     const int64_t limit = g_wait_limit_ns.load();
     const int64_t skip = g_skip_publish.load();
-    bool marked = false;
+    bool marked = false, first = true;
     for (SpliceParams &sp : plans) {
         if (sp.total_tickets == 0)
             continue;
         int64_t nflags = 0;
         for (int i = 0; i < sp.num_seqs; ++i)
             nflags += sp.seq[i].n_shift;
-        KV_CUDA(cudaMemsetAsync(ticket, 0, sizeof(uint32_t), stream));
-        if (nflags > 0)
-            KV_CUDA(cudaMemsetAsync(flags, 0, (size_t)nflags * 4u, stream));
-        TableParams tp{};
-        tp.d_delta = nullptr;
-        for (int i = 0; i < sp.num_seqs; ++i)
-            tp.h_delta[i] = sp.seq[i].delta;
-        tp.units = sp.num_seqs;
-        tp.half = pool->rot_head_dim / 2;
-        tp.head_dim = pool->rot_head_dim;
-        tp.base = pool->rope_base;
-        tp.table = table;
-        KV_CUDA(launch_delta_table(tp, stream));
-        ++t_launches;
+        if (!first) {
+            KV_CUDA(cudaMemsetAsync(ticket, 0, sizeof(uint32_t), stream));
+            if (nflags > 0)
+                KV_CUDA(cudaMemsetAsync(flags, 0, (size_t)nflags * 4u, stream));
+        }
+        first = false;
+        // a launch of at most kInlineTableTiles tiles forms its cos/sin rows
+        // in the blocks themselves (no δ-table kernel); larger ones share the
+        // table, built once
+        sp.inline_table = sp.total_tickets <= kInlineTableTiles ? 1 : 0;
+        sp.rope_base = pool->rope_base;
+        if (!sp.inline_table) {
+            TableParams tp{};
+            tp.d_delta = nullptr;
+            for (int i = 0; i < sp.num_seqs; ++i)
+                tp.h_delta[i] = sp.seq[i].delta;
+            tp.units = sp.num_seqs;
+            tp.half = pool->rot_head_dim / 2;
+            tp.head_dim = pool->rot_head_dim;
+            tp.base = pool->rope_base;
+            tp.table = table;
+            KV_CUDA(launch_delta_table(tp, stream));
+            ++t_launches;
+        }
         sp.pool = view_of(pool);
         sp.block_tables = d_block_tables;
         sp.max_blocks = max_blocks;
@@ -952,13 +977,28 @@ size_t kv_cdc_workspace_size(int64_t total_tokens)
            4 * align256((size_t)blocks * sizeof(int64_t));
 }
 
-kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total_tokens,
-                 const int32_t *d_tokens, uint64_t gear_seed, uint64_t threshold,
-                 uint64_t fp_seed, int64_t max_chunks, int64_t *d_chunk_end,
-                 uint64_t *d_fingerprint, int64_t *d_num_chunks, void *d_workspace,
-                 size_t workspace_bytes, kv_stream_t stream_)
+kv_status kv_cdc_gear_table(uint64_t gear_seed, int64_t vocab, uint64_t *d_table,
+                            kv_stream_t stream)
 {
     t_launches = 0;
+    if (vocab < 0 || vocab > (int64_t(1) << 32) || (vocab > 0 && !d_table) || !aligned_to(d_table, 8))
+        return KV_ERR_INVALID_ARG;
+    KV_CUDA(launch_gear_table(gear_seed, vocab, d_table, reinterpret_cast<cudaStream_t>(stream)));
+    t_launches = vocab > 0 ? 1 : 0;
+    return KV_OK;
+}
+
+kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total_tokens,
+                 const int32_t *d_tokens, uint64_t gear_seed, const uint64_t *d_gear_table,
+                 int64_t gear_table_len, uint64_t threshold, uint64_t fp_seed,
+                 int64_t max_chunks, int64_t *d_chunk_end, uint64_t *d_fingerprint,
+                 int64_t *d_num_chunks, void *d_workspace, size_t workspace_bytes,
+                 kv_stream_t stream_)
+{
+    t_launches = 0;
+    if (gear_table_len < 0 || (gear_table_len > 0 && !d_gear_table) ||
+        !aligned_to(d_gear_table, 8))
+        return KV_ERR_INVALID_ARG;
     if (num_streams < 0 || total_tokens < 0 || max_chunks < 0 || !d_stream_off ||
         !d_num_chunks || (total_tokens > 0 && !d_tokens) ||
         (max_chunks > 0 && (!d_chunk_end || !d_fingerprint)) ||
@@ -979,6 +1019,8 @@ kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total
     p.total = total_tokens;
     p.tokens = d_tokens;
     p.gear_seed = gear_seed;
+    p.gear_table = d_gear_table;
+    p.gear_len = d_gear_table ? gear_table_len : 0;
     p.threshold = threshold;
     p.fp_seed = fp_seed;
     p.max_chunks = max_chunks;

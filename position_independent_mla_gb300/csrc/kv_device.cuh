@@ -449,11 +449,46 @@ static __device__ __noinline__ uint32_t wait_count(const uint32_t *counter, uint
             return v;
         if ((int64_t)(global_ns() - t0) > limit_ns)
             return v;
+        // the awaited tile is usually a fraction of a microsecond away: a
+        // short backoff keeps the detection delay small
         __nanosleep(sleep_ns);
-        if (sleep_ns < 2048)
+        if (sleep_ns < 256)
             sleep_ns <<= 1;
     }
     return ld_acquire(counter);
+}
+
+// ---------------------------------------------------------------------------
+// δ-table entry: cos/sin of δ·θ_j in fp64, stored as two-part fp32
+// ---------------------------------------------------------------------------
+
+// Keep the 16 leading significant bits of a double (truncation).
+__device__ __forceinline__ double lead16(double x)
+{
+    return __longlong_as_double(__double_as_longlong(x) & ~((1ll << 37) - 1));
+}
+
+// (c1, c2, s1, s2) with cos(δθ_j) = c1 + c2 and sin(δθ_j) = s1 + s2, the
+// angle and its cosine / sine formed in fp64, θ_j = base^(-2j/d); c1 and s1
+// keep at most 16 significant bits, so their products with bf16 values are
+// exact in fp32.
+__device__ __forceinline__ float4 delta_entry(int32_t delta, int j, int head_dim, double base)
+{
+    const double theta = pow(base, -2.0 * (double)j / (double)head_dim);
+    const double a = (double)delta * theta;
+    double s, c;
+    sincos(a, &s, &c);
+    const double c1 = lead16(c), s1 = lead16(s);
+    return make_float4((float)c1, (float)(c - c1), (float)s1, (float)(s - s1));
+}
+
+// The same entry behind a call boundary, for kernels that form their table
+// row in a prologue: the fp64 library code then does not weigh on the
+// registers of the kernel's main loop.
+static __device__ __noinline__ float4 delta_entry_call(int32_t delta, int j, int head_dim,
+                                                       double base)
+{
+    return delta_entry(delta, j, head_dim, base);
 }
 
 // Physical slot of logical position pos in a block-table row, or -1 when

@@ -122,6 +122,8 @@ struct SpliceParams {
     int64_t wait_limit_ns;
     int64_t skip_publish; // test hook: this ticket does not publish its reads (-1: none)
     const uint32_t *gate;
+    double rope_base;     // inline_table: every block forms its own cos/sin row
+    int32_t inline_table; // 1: no δ-table kernel ran (small launches)
     int32_t num_seqs;
     SpliceSeq seq[kMaxSeqsPerLaunch];
 };
@@ -231,6 +233,8 @@ struct CdcParams {
     int64_t total;             // tokens
     const int32_t *tokens;
     uint64_t gear_seed, threshold, fp_seed;
+    const uint64_t *gear_table; // G(x) for x < gear_len (nullptr: formed per token)
+    int64_t gear_len;
     int64_t max_chunks;
     int64_t *chunk_end;        // [max_chunks]
     uint64_t *fingerprint;     // [max_chunks]

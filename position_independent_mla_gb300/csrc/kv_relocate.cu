@@ -18,12 +18,6 @@ namespace kvr {
 // δ-table: cos/sin of δ_u·θ_j in fp64, stored as two-part fp32
 // ---------------------------------------------------------------------------
 
-// Keep the 16 leading significant bits of a double (truncation).
-__device__ __forceinline__ double lead16(double x)
-{
-    return __longlong_as_double(__double_as_longlong(x) & ~((1ll << 37) - 1));
-}
-
 __global__ void delta_table_kernel(const __grid_constant__ TableParams p)
 {
     // 64-bit indices and a grid-stride loop: units * half may exceed 2^31
@@ -33,12 +27,7 @@ __global__ void delta_table_kernel(const __grid_constant__ TableParams p)
         const int64_t u = i / p.half;
         const int j = (int)(i % p.half);
         const int32_t delta = p.d_delta ? p.d_delta[u] : p.h_delta[u];
-        const double theta = pow(p.base, -2.0 * (double)j / (double)p.head_dim);
-        const double a = (double)delta * theta;
-        double s, c;
-        sincos(a, &s, &c);
-        const double c1 = lead16(c), s1 = lead16(s);
-        p.table[i] = make_float4((float)c1, (float)(c - c1), (float)s1, (float)(s - s1));
+        p.table[i] = delta_entry(delta, j, p.head_dim, p.base);
     }
 }
 

@@ -127,7 +127,9 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
         }
     }
     for (int j = tid; j < G::kHalf; j += kThreads)
-        stage_cs<G, CsOrder<G, false, IL>::kPacked>(s_cs, j, p.table[(int64_t)q * G::kHalf + j]);
+        stage_cs<G, CsOrder<G, false, IL>::kPacked>(
+            s_cs, j, p.inline_table ? delta_entry_call(S.delta, j, 2 * G::kHalf, p.rope_base)
+                                    : p.table[(int64_t)q * G::kHalf + j]);
     __syncthreads();
 
     const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;

@@ -366,7 +366,9 @@ def test_splice_more_sequences_than_one_launch(orc):
     d = synth.random_directives(431, lens, 0, 100, 0, 120)
     assert _splice_both(orc, ss, dp, bt, glens, olens, d.s_start.tolist(), d.s_end.tolist(),
                         d.stub_len.tolist(), 432, layers=2) == kv.KV_OK
-    assert kv.kv_last_launch_count() == 4
+    # two launches (64 + 6 sequences); both are short enough to form their
+    # cos/sin rows inside the splice kernel, so no δ-table kernel runs
+    assert kv.kv_last_launch_count() == 2
     check_pool(dp, "splice 70 sequences")
 
 

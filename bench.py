@@ -113,7 +113,9 @@ def kernel_sources_hash(workload: str) -> str:
 
 def recorded_traffic(workload: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None when that summary was taken on other kernel sources."""
+    summary (captured on the workload's small case and scaled by the ratio of
+    algorithmic bytes), or None when that summary was taken on other kernel
+    sources."""
     path = os.path.join(ROOT, "profiles", f"{workload}_traffic.txt")
     try:
         kv = dict(line.strip().split("=", 1) for line in open(path)
@@ -122,7 +124,9 @@ def recorded_traffic(workload: str):
         return None
     if kv.get("kernel_sources_sha256_16") != kernel_sources_hash(workload):
         return None
-    return float(kv["dram_bytes_per_launch"])
+    # the figure is scaled from a small case; absent where the small case's
+    # traffic does not grow in proportion to the workload
+    return float(kv["dram_bytes_per_launch"]) if "dram_bytes_per_launch" in kv else None
 
 
 class ClockSampler:
@@ -2136,10 +2140,7 @@ def build_cdc(rank: int, cfg, device: str = "cuda"):
                fps=torch.empty(total, dtype=torch.int64, device=device),
                cnt=torch.zeros(1, dtype=torch.int64, device=device))
     ws = torch.empty(kv.kv_cdc_workspace_size(total), dtype=torch.uint8, device=device)
-    # the vocabulary's Gear values, built once per seed (not part of a step)
-    gear = torch.empty(cfg["vocab"], dtype=torch.int64, device=device)
-    kv.kv_cdc_gear_table(cfg["gear_seed"], cfg["vocab"], gear)
-    return dict(ts=ts, host=host, dev=dev, ws=ws, total=total, cfg=cfg, gear=gear,
+    return dict(ts=ts, host=host, dev=dev, ws=ws, total=total, cfg=cfg,
                 threshold=1 << (64 - cfg["log_mean"]), **out)
 
 
@@ -2149,7 +2150,7 @@ def cdc_call(st, dev=None, stream=None):
     d, c = dev if dev is not None else st["dev"], st["cfg"]
     kv.kv_cdc(st["ts"].num_streams, d["off"], st["total"], d["tok"], c["gear_seed"],
               st["threshold"], c["fp_seed"], st["total"], st["ends"], st["fps"], st["cnt"],
-              st["ws"], stream=stream, gear_table=st["gear"])
+              st["ws"], stream=stream)
     return kv.kv_last_launch_count()
 
 

@@ -350,14 +350,6 @@ kv_status kv_get_device_status(const void *d_workspace, kv_stream_t stream);
 /* Workspace bytes kv_cdc needs for `total_tokens` tokens (256-byte aligned). */
 size_t kv_cdc_workspace_size(int64_t total_tokens);
 
-/* The Gear table of a vocabulary: d_table[x] = G(x) for 0 <= x < vocab (8-byte
- * aligned device array of vocab uint64, the caller's).  G depends only on
- * (gear_seed, x), so one table serves every kv_cdc call with that seed: with
- * it, kv_cdc reads G(x) instead of forming it from SplitMix64 for every staged
- * token.  One kernel. */
-kv_status kv_cdc_gear_table(uint64_t gear_seed, int64_t vocab, uint64_t *d_table,
-                            kv_stream_t stream);
-
 /* Chunk num_streams token streams, concatenated in d_tokens: stream s is
  * tokens d_stream_off[s] .. d_stream_off[s+1]-1 (num_streams+1 int64 device
  * entries, non-decreasing, first 0, last total_tokens; empty streams have no
@@ -367,17 +359,12 @@ kv_status kv_cdc_gear_table(uint64_t gear_seed, int64_t vocab, uint64_t *d_table
  * k < max_chunks, and the number of chunks to the device scalar
  * *d_num_chunks.  More chunks than max_chunks set the device status
  * KV_ERR_CAPACITY (total_tokens chunks always fit); offsets that do not start
- * at 0 or end at total_tokens set KV_ERR_OUT_OF_RANGE.  d_gear_table (NULL:
- * none) is a table that kv_cdc_gear_table built with the same gear_seed for
- * gear_table_len ids: ids below gear_table_len take G from it, the others
- * (and every id without a table) form it from SplitMix64; the results are
- * the same either way.  Three kernels. */
+ * at 0 or end at total_tokens set KV_ERR_OUT_OF_RANGE.  Three kernels. */
 kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total_tokens,
-                 const int32_t *d_tokens, uint64_t gear_seed, const uint64_t *d_gear_table,
-                 int64_t gear_table_len, uint64_t threshold, uint64_t fp_seed,
-                 int64_t max_chunks, int64_t *d_chunk_end, uint64_t *d_fingerprint,
-                 int64_t *d_num_chunks, void *d_workspace, size_t workspace_bytes,
-                 kv_stream_t stream);
+                 const int32_t *d_tokens, uint64_t gear_seed, uint64_t threshold,
+                 uint64_t fp_seed, int64_t max_chunks, int64_t *d_chunk_end,
+                 uint64_t *d_fingerprint, int64_t *d_num_chunks, void *d_workspace,
+                 size_t workspace_bytes, kv_stream_t stream);
 
 /* Fingerprints of arbitrary token ranges: d_fingerprint[k] = XXH64 of tokens
  * d_start[k] .. d_end[k]-1 (device int64 arrays, 0 <= start <= end <=

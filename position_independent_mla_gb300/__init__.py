@@ -118,9 +118,8 @@ def load(build_if_missing: bool = False) -> C.CDLL:
         "kv_relocate_noalloc": (i32, [P, P, i32, i64, vp, vp, vp, vp, vp, vp, i32, i32, PP,
                                       C.POINTER(C.c_int32), vp]),
         "kv_cdc_workspace_size": (sz, [i64]),
-        "kv_cdc_gear_table": (i32, [C.c_uint64, i64, vp, vp]),
-        "kv_cdc": (i32, [i32, vp, i64, vp, C.c_uint64, vp, i64, C.c_uint64, C.c_uint64, i64, vp,
-                         vp, vp, vp, sz, vp]),
+        "kv_cdc": (i32, [i32, vp, i64, vp, C.c_uint64, C.c_uint64, C.c_uint64, i64, vp, vp, vp,
+                         vp, sz, vp]),
         "kv_fingerprint": (i32, [i64, vp, vp, i64, vp, C.c_uint64, vp, vp, sz, vp]),
         "kv_status_string": (C.c_char_p, [i32]),
         "kv_version": (i32, []),
@@ -341,33 +340,17 @@ def kv_cdc_workspace_size(total_tokens: int) -> int:
     return int(load().kv_cdc_workspace_size(int(total_tokens)))
 
 
-def kv_cdc_gear_table(gear_seed: int, vocab: int, table: torch.Tensor, stream=None,
-                      check: bool = True) -> int:
-    """Fill ``table`` (device int64 tensor holding uint64 bits, at least
-    ``vocab`` entries) with the Gear values G(0) .. G(vocab - 1)."""
-    assert table.dtype == torch.int64 and table.numel() >= vocab
-    st = load().kv_cdc_gear_table(int(gear_seed) & (2**64 - 1), int(vocab), table.data_ptr(),
-                                  _stream(stream))
-    if check:
-        _check(st, "kv_cdc_gear_table")
-    return st
-
-
 def kv_cdc(num_streams: int, stream_off, total_tokens: int, tokens, gear_seed: int,
            threshold: int, fp_seed: int, max_chunks: int, chunk_end, fingerprint, num_chunks,
-           ws: torch.Tensor, stream=None, check: bool = True, gear_table=None) -> int:
+           ws: torch.Tensor, stream=None, check: bool = True) -> int:
     """Content-defined chunking (Irminsul §2.2); device tensors: stream_off
     int64 [S+1], tokens int32, chunk_end int64 and fingerprint (uint64 bits in
-    an int64 tensor) [max_chunks], num_chunks int64 [1].  ``gear_table``: an
-    optional table from kv_cdc_gear_table with the same ``gear_seed`` (its
-    length is the vocabulary it covers)."""
+    an int64 tensor) [max_chunks], num_chunks int64 [1]."""
     m = 2**64 - 1
-    gt = None if gear_table is None else gear_table.data_ptr()
-    gl = 0 if gear_table is None else int(gear_table.numel())
     st = load().kv_cdc(int(num_streams), _ptr(stream_off), int(total_tokens), _ptr(tokens),
-                       int(gear_seed) & m, gt, gl, int(threshold) & m, int(fp_seed) & m,
-                       int(max_chunks), _ptr(chunk_end), _ptr(fingerprint), _ptr(num_chunks),
-                       ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream))
+                       int(gear_seed) & m, int(threshold) & m, int(fp_seed) & m, int(max_chunks),
+                       _ptr(chunk_end), _ptr(fingerprint), _ptr(num_chunks), ws.data_ptr(),
+                       ws.numel() * ws.element_size(), _stream(stream))
     if check:
         _check(st, "kv_cdc")
     return st

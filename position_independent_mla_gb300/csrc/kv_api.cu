@@ -19,6 +19,10 @@ using namespace kvr;
 namespace {
 
 constexpr int64_t kDefaultWaitLimitNs = 2000000000ll;
+// A splice launch of few tiles cuts every tile's layers into groups (units of
+// their own) until it has about this many units: some 7 waves of 4 blocks on
+// each of 152 SMs, so that the last, partly filled wave costs little.
+constexpr int64_t kUnitsTarget = 4096;
 // Splice launches of at most this many tiles (a wave or two) form their
 // cos/sin rows inside the splice kernel instead of launching the δ-table
 // kernel: each block spends a few fp64 sincos on its prologue, which only
@@ -621,40 +625,70 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
             remap[q] = h_s_start[q] % B == 0 && h_s_end[q] % B == 0 && h_stub_len[q] % B == 0 &&
                        h_stub_len[q] != h_s_end[q] - h_s_start[q];
 
-    // plan: launches of up to kMaxSeqsPerLaunch sequences each
+    // plan: launches of up to kMaxSeqsPerLaunch sequences each; a launch of
+    // few tiles cuts every tile's layers into groups, each its own ticketed
+    // unit, so that short edits still fill the GPU (max_groups 1: whole tiles)
     const int T = inplace_tile_rows(kind);
     std::vector<SpliceParams> plans;
     int64_t stub_base = 0, max_flags = 0;
-    for (int q0 = 0; q0 < num_seqs; q0 += kMaxSeqsPerLaunch) {
-        SpliceParams sp{};
-        sp.num_seqs = std::min(kMaxSeqsPerLaunch, num_seqs - q0);
-        int64_t tickets = 0, flags = 0;
-        for (int i = 0; i < sp.num_seqs; ++i) {
-            const int q = q0 + i;
-            SpliceSeq &S = sp.seq[i];
-            S.s_start = h_s_start[q];
-            S.s_end = h_s_end[q];
-            S.seq_len = h_seq_lens[q];
-            S.n_r = h_stub_len[q];
-            S.delta = S.n_r - (S.s_end - S.s_start);
-            const int64_t down = S.seq_len - S.s_end;
-            S.n_shift = (S.delta == 0 || remap[q]) ? 0 : (int32_t)((down + T - 1) / T);
-            S.n_stub = remap[q] ? 0 : (S.n_r + T - 1) / T;
-            S.bt_row = q;
-            S.ticket_base = tickets;
-            S.flag_base = flags;
-            S.stub_base = stub_base;
-            tickets += S.n_shift + S.n_stub;
-            flags += S.n_shift;
-            stub_base += S.n_r;
+    auto make_plans = [&](int32_t max_groups) {
+        plans.clear();
+        stub_base = 0;
+        max_flags = 0;
+        for (int q0 = 0; q0 < num_seqs; q0 += kMaxSeqsPerLaunch) {
+            SpliceParams sp{};
+            sp.num_seqs = std::min(kMaxSeqsPerLaunch, num_seqs - q0);
+            int64_t tickets = 0, flags = 0;
+            for (int i = 0; i < sp.num_seqs; ++i) {
+                const int q = q0 + i;
+                SpliceSeq &S = sp.seq[i];
+                S.s_start = h_s_start[q];
+                S.s_end = h_s_end[q];
+                S.seq_len = h_seq_lens[q];
+                S.n_r = h_stub_len[q];
+                S.delta = S.n_r - (S.s_end - S.s_start);
+                const int64_t down = S.seq_len - S.s_end;
+                S.n_shift = (S.delta == 0 || remap[q]) ? 0 : (int32_t)((down + T - 1) / T);
+                S.n_stub = remap[q] ? 0 : (S.n_r + T - 1) / T;
+                S.bt_row = q;
+                S.stub_base = stub_base;
+                stub_base += S.n_r;
+                tickets += S.n_shift + S.n_stub;
+            }
+            // layer groups: enough units for about kUnitsTarget blocks
+            const int32_t L = pool->num_layers;
+            int32_t groups = (int32_t)std::min<int64_t>(
+                std::min<int64_t>(L, max_groups),
+                std::max<int64_t>(1, (kUnitsTarget + std::max<int64_t>(tickets, 1) - 1) /
+                                         std::max<int64_t>(tickets, 1)));
+            const int32_t per = (L + groups - 1) / groups;
+            groups = (L + per - 1) / per;
+            sp.layer_groups = groups;
+            sp.group_layers = per;
+            tickets = 0;
+            for (int i = 0; i < sp.num_seqs; ++i) {
+                SpliceSeq &S = sp.seq[i];
+                S.ticket_base = tickets;
+                S.flag_base = flags;
+                tickets += (int64_t)(S.n_shift + S.n_stub) * groups;
+                flags += (int64_t)S.n_shift * groups;
+            }
+            sp.total_tickets = tickets;
+            max_flags = std::max(max_flags, flags);
+            plans.push_back(sp);
         }
-        sp.total_tickets = tickets;
-        max_flags = std::max(max_flags, flags);
-        plans.push_back(sp);
+    };
+    make_plans(pool->num_layers);
+    const bool check = g_debug_checks.load() != 0;
+    {
+        // a workspace too small for these groups' counters: whole tiles
+        const size_t tb = table_bytes(pool, std::min(num_seqs, kMaxSeqsPerLaunch));
+        if (workspace_bytes < kHeaderBytes + tb + align256((size_t)max_flags * 4u) +
+                                  (check ? debug_bytes(pool, num_seqs) : 0))
+            make_plans(1);
     }
     const size_t tbytes = table_bytes(pool, std::min(num_seqs, kMaxSeqsPerLaunch));
     const size_t need = kHeaderBytes + tbytes + align256((size_t)max_flags * 4u);
-    const bool check = g_debug_checks.load() != 0;
     kv_status st =
         ws_ok(d_workspace, workspace_bytes, need + (check ? debug_bytes(pool, num_seqs) : 0));
     if (st != KV_OK)
@@ -672,7 +706,7 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
     for (const SpliceParams &sp : plans)
         if (sp.total_tickets > 0) {
             for (int i = 0; i < sp.num_seqs; ++i)
-                first_flags += (size_t)sp.seq[i].n_shift;
+                first_flags += (size_t)sp.seq[i].n_shift * (size_t)sp.layer_groups;
             break;
         }
     KV_CUDA(cudaMemsetAsync(w, 0, kHeaderBytes + first_flags * 4u, stream));
@@ -698,7 +732,7 @@ kv_status kv_splice(const kv_pool_desc *pool, int32_t num_seqs, int32_t *d_block
             continue;
         int64_t nflags = 0;
         for (int i = 0; i < sp.num_seqs; ++i)
-            nflags += sp.seq[i].n_shift;
+            nflags += (int64_t)sp.seq[i].n_shift * sp.layer_groups;
         if (!first) {
             KV_CUDA(cudaMemsetAsync(ticket, 0, sizeof(uint32_t), stream));
             if (nflags > 0)
@@ -977,28 +1011,13 @@ size_t kv_cdc_workspace_size(int64_t total_tokens)
            4 * align256((size_t)blocks * sizeof(int64_t));
 }
 
-kv_status kv_cdc_gear_table(uint64_t gear_seed, int64_t vocab, uint64_t *d_table,
-                            kv_stream_t stream)
-{
-    t_launches = 0;
-    if (vocab < 0 || vocab > (int64_t(1) << 32) || (vocab > 0 && !d_table) || !aligned_to(d_table, 8))
-        return KV_ERR_INVALID_ARG;
-    KV_CUDA(launch_gear_table(gear_seed, vocab, d_table, reinterpret_cast<cudaStream_t>(stream)));
-    t_launches = vocab > 0 ? 1 : 0;
-    return KV_OK;
-}
-
 kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total_tokens,
-                 const int32_t *d_tokens, uint64_t gear_seed, const uint64_t *d_gear_table,
-                 int64_t gear_table_len, uint64_t threshold, uint64_t fp_seed,
-                 int64_t max_chunks, int64_t *d_chunk_end, uint64_t *d_fingerprint,
-                 int64_t *d_num_chunks, void *d_workspace, size_t workspace_bytes,
-                 kv_stream_t stream_)
+                 const int32_t *d_tokens, uint64_t gear_seed, uint64_t threshold,
+                 uint64_t fp_seed, int64_t max_chunks, int64_t *d_chunk_end,
+                 uint64_t *d_fingerprint, int64_t *d_num_chunks, void *d_workspace,
+                 size_t workspace_bytes, kv_stream_t stream_)
 {
     t_launches = 0;
-    if (gear_table_len < 0 || (gear_table_len > 0 && !d_gear_table) ||
-        !aligned_to(d_gear_table, 8))
-        return KV_ERR_INVALID_ARG;
     if (num_streams < 0 || total_tokens < 0 || max_chunks < 0 || !d_stream_off ||
         !d_num_chunks || (total_tokens > 0 && !d_tokens) ||
         (max_chunks > 0 && (!d_chunk_end || !d_fingerprint)) ||
@@ -1019,8 +1038,6 @@ kv_status kv_cdc(int32_t num_streams, const int64_t *d_stream_off, int64_t total
     p.total = total_tokens;
     p.tokens = d_tokens;
     p.gear_seed = gear_seed;
-    p.gear_table = d_gear_table;
-    p.gear_len = d_gear_table ? gear_table_len : 0;
     p.threshold = threshold;
     p.fp_seed = fp_seed;
     p.max_chunks = max_chunks;

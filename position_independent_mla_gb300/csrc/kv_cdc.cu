@@ -29,8 +29,6 @@
 //      lanes, one XXH64 accumulator each (shared memory, global memory for a
 //      part that starts further back).
 // kv_fingerprint runs fingerprint_kernel: one thread per range.
-#include <algorithm>
-
 #include "kv_device.cuh"
 #include "kv_launch.h"
 
@@ -246,8 +244,7 @@ __global__ void __launch_bounds__(kThreadsCdc) cdc_flags_kernel(const __grid_con
         for (int k = 0; k < kBatch; ++k) {
             const int64_t q = lo + tid + (k0 + k) * kThreadsCdc;
             if (k0 + k < kPer && q >= 0 && q < hi)
-                s_g[staged(tid + (k0 + k) * kThreadsCdc)] =
-                    x[k] < p.gear_len ? __ldg(p.gear_table + x[k]) : gear_value(p.gear_seed, x[k]);
+                s_g[staged(tid + (k0 + k) * kThreadsCdc)] = gear_value(p.gear_seed, x[k]);
         }
     }
     // positions lo .. hi, both ends included: a start at hi ends the stream before it
@@ -543,22 +540,6 @@ __global__ void __launch_bounds__(kThreadsCdc) fingerprint_kernel(FingerprintPar
 } // namespace
 
 int64_t cdc_blocks(int64_t total) { return (total + kTileCdc - 1) / kTileCdc; }
-
-__global__ void gear_table_kernel(uint64_t seed, int64_t vocab, uint64_t *table)
-{
-    for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < vocab;
-         x += (int64_t)gridDim.x * blockDim.x)
-        table[x] = gear_value(seed, (uint32_t)x);
-}
-
-cudaError_t launch_gear_table(uint64_t seed, int64_t vocab, uint64_t *table, cudaStream_t stream)
-{
-    if (vocab <= 0)
-        return cudaSuccess;
-    const int64_t blocks = std::min<int64_t>((vocab + 255) / 256, 152 * 8);
-    gear_table_kernel<<<(unsigned)blocks, 256, 0, stream>>>(seed, vocab, table);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_cdc(const CdcParams &p, cudaStream_t stream)
 {

@@ -99,11 +99,11 @@ struct RelocParams {
 struct SpliceSeq {
     int32_t s_start, s_end, seq_len, n_r;
     int32_t delta;   // n_r - (s_end - s_start)
-    int32_t n_shift; // shift tiles (each covers all layers)
+    int32_t n_shift; // shift tiles (each covers all layers, in layer_groups units)
     int32_t n_stub;  // stub tiles
     int32_t bt_row;  // block-table row
     int64_t ticket_base;
-    int64_t flag_base; // per-tile "layers read" counters of this sequence: [n_shift]
+    int64_t flag_base; // per-unit "layers read" counters of this sequence: [n_shift][groups]
     int64_t stub_base; // first stub row of this sequence
 };
 
@@ -124,6 +124,8 @@ struct SpliceParams {
     const uint32_t *gate;
     double rope_base;     // inline_table: every block forms its own cos/sin row
     int32_t inline_table; // 1: no δ-table kernel ran (small launches)
+    int32_t layer_groups; // a tile's layers are cut into this many units ...
+    int32_t group_layers; // ... of this many layers (the last may be shorter)
     int32_t num_seqs;
     SpliceSeq seq[kMaxSeqsPerLaunch];
 };
@@ -233,8 +235,6 @@ struct CdcParams {
     int64_t total;             // tokens
     const int32_t *tokens;
     uint64_t gear_seed, threshold, fp_seed;
-    const uint64_t *gear_table; // G(x) for x < gear_len (nullptr: formed per token)
-    int64_t gear_len;
     int64_t max_chunks;
     int64_t *chunk_end;        // [max_chunks]
     uint64_t *fingerprint;     // [max_chunks]

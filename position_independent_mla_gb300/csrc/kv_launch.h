@@ -36,7 +36,6 @@ cudaError_t launch_dup_block_check(const DupBlockParams &p, cudaStream_t stream)
 // Content-defined chunking: flags, scan, emit (+ fingerprint) kernels.
 int64_t cdc_blocks(int64_t total_tokens);
 cudaError_t launch_cdc(const CdcParams &p, cudaStream_t stream);
-cudaError_t launch_gear_table(uint64_t seed, int64_t vocab, uint64_t *table, cudaStream_t stream);
 cudaError_t launch_fingerprint(const FingerprintParams &p, cudaStream_t stream);
 constexpr int kCdcLaunches = 3;
 

@@ -33,7 +33,9 @@ namespace kvr {
 
 constexpr uint32_t kWarps = kThreads / 32;
 
-template <class G, bool IL>
+// GR: the launch cuts tiles into layer groups (p.layer_groups > 1); without
+// it the unit is the whole tile and the loop runs over every layer.
+template <class G, bool IL, bool GR>
 __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const __grid_constant__ SpliceParams p)
 {
     __shared__ uint32_t s_ticket;
@@ -62,12 +64,18 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
     while (q + 1 < p.num_seqs && p.seq[q + 1].ticket_base <= t)
         ++q;
     const SpliceSeq &S = p.seq[q];
-    const int64_t k = t - S.ticket_base;
-    const bool shift = k < S.n_shift;
+    // this unit: tile k of the sequence, layers [l0, l1) (group g of its layers)
+    const int64_t u = t - S.ticket_base;
+    const int32_t NG = GR ? p.layer_groups : 1;
+    const int64_t shift_units = (int64_t)S.n_shift * NG;
+    const bool shift = u < shift_units;
+    const int64_t k = shift ? u / NG : S.n_shift + (u - shift_units) / NG;
+    const int g = (int)(shift ? u % NG : (u - shift_units) % NG);
     const int32_t *bt = p.block_tables + (int64_t)S.bt_row * p.max_blocks;
     const int32_t B = p.pool.block;
     const int64_t nb = p.pool.num_blocks;
-    const int L = p.pool.num_layers;
+    const int l0 = GR ? g * p.group_layers : 0;
+    const int l1 = GR ? min(p.pool.num_layers, l0 + p.group_layers) : p.pool.num_layers;
 
     // positions (shift tile) or stub rows (stub tile) covered: [lo, hi)
     int64_t lo, hi;
@@ -134,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
 
     const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;
     PatchAt none{nullptr, 0, nullptr, nullptr};
-    for (int l = 0; l < L; ++l) {
+    for (int l = l0; l < l1; ++l) {
         const RowsAt pool_l{p.pool.copy + l * p.pool.copy_ls, p.pool.copy_ss,
                             p.pool.rot + l * p.pool.rot_ls, p.pool.rot_ss};
         const RowsAt from = shift ? pool_l
@@ -157,15 +165,16 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
         // overwritten only by itself and by later tiles)
         __syncwarp();
         if (shift && (tid & 31) == 0 && t != p.skip_publish)
-            red_release_add(p.flags + S.flag_base + k, 1u);
-        const uint32_t want = ((uint32_t)l + 1u) * kWarps; // every warp has read layer l
+            red_release_add(p.flags + S.flag_base + k * NG + g, 1u);
+        // every warp of the same layer group of a tile has read layer l
+        const uint32_t want = ((uint32_t)(l - l0) + 1u) * kWarps;
         if (tid == 0 && !s_abort) {
             // the tiles this one overwrites must have read layer l
             for (int d = 0; d < 2; ++d) {
                 if (s_dep[d] < 0 || s_seen[d] >= want)
                     continue;
-                const uint32_t seen =
-                    wait_count(p.flags + S.flag_base + s_dep[d], want, p.wait_limit_ns);
+                const uint32_t seen = wait_count(p.flags + S.flag_base + s_dep[d] * NG + g, want,
+                                                 p.wait_limit_ns);
                 if (seen < want) {
                     set_status(p.status, kStatusTimeout);
                     s_abort = 1;
@@ -189,9 +198,11 @@ cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stre
     const unsigned blocks = (unsigned)p.total_tickets;
     return with_inplace_geo(kind, [&](auto g) {
         return with_bool(p.pool.il != 0, [&](auto il) {
-            splice_kernel<typename decltype(g)::type, decltype(il)::value>
-                <<<blocks, kThreads, 0, stream>>>(p);
-            return cudaGetLastError();
+            return with_bool(p.layer_groups > 1, [&](auto gr) {
+                splice_kernel<typename decltype(g)::type, decltype(il)::value,
+                              decltype(gr)::value><<<blocks, kThreads, 0, stream>>>(p);
+                return cudaGetLastError();
+            });
         });
     });
 }

@@ -133,19 +133,9 @@ def test_cdc_host_checks(lib):
                      C.c_void_p(256), C.c_void_p(256), ws, check=False) == kv.KV_ERR_INVALID_ARG
     # workspace too small for the token count
     small = C.c_void_p(1 << 24)
-    assert lib.kv_cdc(1, C.c_void_p(256), 1 << 20, C.c_void_p(256), 0, None, 0, 0, 0, 10,
+    assert lib.kv_cdc(1, C.c_void_p(256), 1 << 20, C.c_void_p(256), 0, 0, 0, 10,
                       C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), small, 256,
                       None) == kv.KV_ERR_WORKSPACE
-    # a Gear table: length without a table, misaligned table
-    assert lib.kv_cdc(1, C.c_void_p(256), 10, C.c_void_p(256), 0, None, 5, 0, 0, 10,
-                      C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), small, 1 << 20,
-                      None) == kv.KV_ERR_INVALID_ARG
-    assert lib.kv_cdc(1, C.c_void_p(256), 10, C.c_void_p(256), 0, C.c_void_p(260), 5, 0, 0,
-                      10, C.c_void_p(256), C.c_void_p(256), C.c_void_p(256), small, 1 << 20,
-                      None) == kv.KV_ERR_INVALID_ARG
-    assert lib.kv_cdc_gear_table(0, -1, C.c_void_p(256), None) == kv.KV_ERR_INVALID_ARG
-    assert lib.kv_cdc_gear_table(0, 10, None, None) == kv.KV_ERR_INVALID_ARG
-    assert lib.kv_cdc_gear_table(0, 10, C.c_void_p(260), None) == kv.KV_ERR_INVALID_ARG
     assert kv.kv_fingerprint(3, None, None, 10, None, 0, None, ws,
                              check=False) == kv.KV_ERR_INVALID_ARG
 

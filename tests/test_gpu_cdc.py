@@ -129,38 +129,3 @@ def test_fixed_window_fingerprints(orc):
     assert kv.kv_get_device_status(ws) == kv.KV_OK
     assert np.array_equal(out.cpu().numpy().view(np.uint64), want)
     assert kv.kv_last_launch_count() == 1
-
-
-def test_gear_table_matches_the_oracle_generator(orc):
-    seed = 0x1234_5678_9ABC_DEF0
-    vocab = 5000
-    table = torch.zeros(vocab, dtype=torch.int64, device="cuda")
-    kv.kv_cdc_gear_table(seed, vocab, table)
-    got = table.cpu().numpy().view(np.uint64)
-    for x in list(range(0, 40)) + list(range(vocab - 40, vocab)) + [1234, 2500, 4097]:
-        assert int(got[x]) == orc.splitmix64_at(seed, x), x
-
-
-@pytest.mark.parametrize("vocab", [1, 700, 129280])
-def test_cdc_with_a_gear_table_matches_oracle(orc, vocab):
-    # ids below the table's length read it, the others form G themselves
-    gear_seed, threshold, fp_seed = 99, 2**58, 5
-    ts = synth.token_streams(77, RAGGED, vocab=2000, shared_segments=3, segment_lo=50,
-                             segment_hi=3000)
-    total = len(ts.tokens)
-    table = torch.zeros(vocab, dtype=torch.int64, device="cuda")
-    kv.kv_cdc_gear_table(gear_seed, vocab, table)
-    off = torch.from_numpy(ts.stream_off).cuda()
-    tok = torch.from_numpy(ts.tokens).cuda()
-    ends = torch.full((total,), -1, dtype=torch.int64, device="cuda")
-    fps = torch.zeros((total,), dtype=torch.int64, device="cuda")
-    cnt = torch.full((1,), -1, dtype=torch.int64, device="cuda")
-    ws = torch.empty(kv.kv_cdc_workspace_size(total), dtype=torch.uint8, device="cuda")
-    kv.kv_cdc(ts.num_streams, off, total, tok, gear_seed, threshold, fp_seed, total, ends, fps,
-              cnt, ws, gear_table=table)
-    assert kv.kv_get_device_status(ws) == kv.KV_OK
-    w_ends, w_fps, w_n = orc.cdc(ts.stream_off, ts.tokens, gear_seed, threshold, fp_seed)
-    n = int(cnt.item())
-    assert n == w_n
-    assert np.array_equal(ends[:n].cpu().numpy(), w_ends)
-    assert np.array_equal(fps[:n].cpu().numpy().view(np.uint64), w_fps)

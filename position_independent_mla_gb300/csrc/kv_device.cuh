@@ -414,6 +414,19 @@ __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v)
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// Named barrier `id` over `count` threads of the block: bar_arrive signals
+// (and orders the caller's earlier memory accesses before the waiters'
+// later ones) without waiting; bar_wait_all waits for the phase to complete.
+__device__ __forceinline__ void bar_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void bar_wait_all(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Spin until *flag != 0, for at most limit_ns of wall time and at most a
 // fixed number of polls (the poll cap bounds the wait even if the timer
 // misbehaves).  Returns false if the wait ran out.

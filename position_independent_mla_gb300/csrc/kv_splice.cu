@@ -13,11 +13,14 @@
 // at most two earlier tiles.  Each block takes a ticket from an atomic
 // counter (so tickets are handed out in launch order, and every tile a block
 // waits for belongs to a block that is already running).  Every shift tile
-// owns a counter of (layer, warp) reads, each warp adding one with a release
-// reduction once its loads of a layer have landed, so layer l is read when
-// the counter reaches 8 (l + 1).  A warp publishes at once: reading needs
-// nothing, since a tile's source rows are overwritten only by itself and by
-// later tiles.  Then thread 0 makes sure (acquire, bounded) that the tiles
+// owns a counter of layer reads: once the eight row-moving warps' loads of a
+// layer have landed, a ninth warp of the block, which moves no rows and so
+// has no stores of its own in flight for its release to wait on, adds 8
+// with a release reduction, so layer l is read when the counter reaches
+// 8 (l + 1).  The warps signal it through a named barrier without waiting,
+// and it publishes at once: reading needs nothing, since a tile's source
+// rows are overwritten only by itself and by later tiles.  Then thread 0
+// makes sure (acquire, bounded) that the tiles
 // it overwrites have read this layer -- a value seen once covers all layers
 // up to it, so a dependency far behind costs one poll for the whole tile --
 // and after one barrier the rows are stored.  Because reads are published before any wait,
@@ -31,12 +34,29 @@
 
 namespace kvr {
 
-constexpr uint32_t kWarps = kThreads / 32;
+constexpr uint32_t kWarps = kThreads / 32; // row-moving warps of a splice block
+// threads of a splice block: the row-moving warps, then the publishing warp
+constexpr int kSpliceThreads = kThreads + 32;
+constexpr uint32_t kReadBar = 1; // named barrier: the warps' loads of a layer have landed
+// resident blocks per SM to aim for: three 288-thread blocks leave each
+// thread enough registers to hold its rows without local-memory spills
+constexpr int kSpliceMinBlocks = 3;
+
+// The publishing warp's part of one layer: wait until every row-moving warp
+// has read the layer, add their 8 reads to `flag` with a release reduction
+// (one lane; none when flag is null), then join the block's barrier.
+__device__ __forceinline__ void publish_layer(uint32_t *flag)
+{
+    bar_wait_all(kReadBar, kSpliceThreads);
+    if (flag != nullptr && (threadIdx.x & 31) == 0)
+        red_release_add(flag, kWarps);
+    __syncthreads();
+}
 
 // GR: the launch cuts tiles into layer groups (p.layer_groups > 1); without
 // it the unit is the whole tile and the loop runs over every layer.
 template <class G, bool IL, bool GR>
-__global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const __grid_constant__ SpliceParams p)
+__global__ void __launch_bounds__(kSpliceThreads, kSpliceMinBlocks) splice_kernel(const __grid_constant__ SpliceParams p)
 {
     __shared__ uint32_t s_ticket;
     __shared__ volatile int32_t s_abort; // 0 -> 1 once a wait ran out; never reset
@@ -140,6 +160,14 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
                                     : p.table[(int64_t)q * G::kHalf + j]);
     __syncthreads();
 
+    if (tid >= kThreads) {
+        // the publishing warp: this unit's read counter, once per layer
+        uint32_t *flag = shift && t != p.skip_publish ? p.flags + S.flag_base + k * NG + g
+                                                       : nullptr;
+        for (int l = l0; l < l1; ++l)
+            publish_layer(flag);
+        return;
+    }
     const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;
     PatchAt none{nullptr, 0, nullptr, nullptr};
     for (int l = l0; l < l1; ++l) {
@@ -159,13 +187,11 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) splice_kernel(const _
         const uint32_t f = fold_tile<G>(regs);
         if (p.total_tickets < 0)
             s_sink = f;
-        // this warp's share of layer l is in registers: publish it now (one
-        // increment per warp), before waiting on anyone, so that a tile's
+        // this warp's share of layer l is in registers: let the publishing
+        // warp count it now, before waiting on anyone, so that a tile's
         // progress never waits on the tiles behind it (its source rows are
         // overwritten only by itself and by later tiles)
-        __syncwarp();
-        if (shift && (tid & 31) == 0 && t != p.skip_publish)
-            red_release_add(p.flags + S.flag_base + k * NG + g, 1u);
+        bar_arrive(kReadBar, kSpliceThreads);
         // every warp of the same layer group of a tile has read layer l
         const uint32_t want = ((uint32_t)(l - l0) + 1u) * kWarps;
         if (tid == 0 && !s_abort) {
@@ -200,7 +226,7 @@ cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stre
         return with_bool(p.pool.il != 0, [&](auto il) {
             return with_bool(p.layer_groups > 1, [&](auto gr) {
                 splice_kernel<typename decltype(g)::type, decltype(il)::value,
-                              decltype(gr)::value><<<blocks, kThreads, 0, stream>>>(p);
+                              decltype(gr)::value><<<blocks, kSpliceThreads, 0, stream>>>(p);
                 return cudaGetLastError();
             });
         });
@@ -215,14 +241,14 @@ cudaError_t launch_splice(const SpliceParams &p, RowKind kind, cudaStream_t stre
 // so that every tile a tile overwrites comes earlier: rows moving down in
 // ascending order, rows moving up in descending order, stubs last (the map
 // is monotone, so rows moving down and rows moving up never overlap).  The
-// protocol is the splice's: tickets, per-warp release counts of the layers
-// read, bounded acquire waits on the (at most two ranges of) earlier tiles a
-// tile overwrites, one barrier per layer.  Every row is read once and rounded
+// protocol is the splice's: tickets, release counts of the layers read (from
+// the publishing warp), bounded acquire waits on the (at most two ranges of)
+// earlier tiles a tile overwrites, one barrier per layer.  Every row is read once and rounded
 // once, its rotary part turned by its total shift.
 // ---------------------------------------------------------------------------
 
 template <class G, bool IL>
-__global__ void __launch_bounds__(kThreads, G::kMinBlocks)
+__global__ void __launch_bounds__(kSpliceThreads, kSpliceMinBlocks)
 splice_composed_kernel(const __grid_constant__ ComposedParams p)
 {
     __shared__ uint32_t s_ticket;
@@ -271,6 +297,13 @@ splice_composed_kernel(const __grid_constant__ ComposedParams p)
                                                      p.table[(int64_t)tile.unit * G::kHalf + j]);
     __syncthreads();
 
+    if (tid >= kThreads) {
+        // the publishing warp: this tile's read counter, once per layer
+        uint32_t *flag = !tile.stub && t != p.skip_publish ? p.flags + t : nullptr;
+        for (int l = 0; l < L; ++l)
+            publish_layer(flag);
+        return;
+    }
     const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;
     PatchAt none{nullptr, 0, nullptr, nullptr};
     for (int l = 0; l < L; ++l) {
@@ -289,10 +322,8 @@ splice_composed_kernel(const __grid_constant__ ComposedParams p)
         const uint32_t f = fold_tile<G>(regs);
         if (p.num_tiles < 0)
             s_sink = f;
-        // this warp's share of layer l is read: publish before waiting
-        __syncwarp();
-        if (!tile.stub && (tid & 31) == 0 && t != p.skip_publish)
-            red_release_add(p.flags + t, 1u);
+        // this warp's share of layer l is read: counted before any wait
+        bar_arrive(kReadBar, kSpliceThreads);
         const uint32_t want = ((uint32_t)l + 1u) * kWarps;
         if (tid == 0 && !s_abort) {
             for (int r = 0; r < 2 && !s_abort; ++r) {
@@ -328,7 +359,7 @@ cudaError_t launch_splice_composed(const ComposedParams &p, RowKind kind, cudaSt
     return with_inplace_geo(kind, [&](auto g) {
         return with_bool(p.pool.il != 0, [&](auto il) {
             splice_composed_kernel<typename decltype(g)::type, decltype(il)::value>
-                <<<blocks, kThreads, 0, stream>>>(p);
+                <<<blocks, kSpliceThreads, 0, stream>>>(p);
             return cudaGetLastError();
         });
     });

@@ -440,9 +440,12 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(con
         s_src[tid] = (!down && slot >= 0) ? tid : -1;
         s_ident[tid] = down ? 0 : 1;
     }
+    // downstream tiles turn only the rotary part: pair-packed for every row
+    // kind; stub tiles are written unrotated (identity rows)
+    constexpr bool kPack = CsOrder<G, false, IL, true>::kPacked;
     if (down)
         for (int j = tid; j < G::kHalf; j += kThreads)
-            stage_cs<G, CsOrder<G, false, IL>::kPacked>(s_cs, j, p.table[(int64_t)q * G::kHalf + j]);
+            stage_cs<G, kPack>(s_cs, j, p.table[(int64_t)q * G::kHalf + j]);
     __syncthreads();
 
     const int64_t copy_row_bytes = (int64_t)G::CV * 16, rot_row_bytes = (int64_t)G::kRotW * 16;
@@ -453,8 +456,10 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(con
     };
     if (down) {
         // rotary part only, in place; rows of different layers are
-        // independent, so LB layers of loads are in flight at once
-        constexpr int LB = G::kRotPer >= 4 ? 1 : 8 / G::kRotPer;
+        // independent, so LB layers of loads are in flight at once (four
+        // 16-byte loads per thread: with the pair-packed rotation eight
+        // layers spilled registers and measured slower)
+        constexpr int LB = G::kRotPer >= 4 ? 1 : 4 / G::kRotPer;
         const int Lc = p.pool.num_layers;
         for (int l0 = 0; l0 < Lc; l0 += LB) {
             TileRegs<G> regs[LB];
@@ -465,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, G::kMinBlocks) remap_data_kernel(con
 #pragma unroll
             for (int b = 0; b < LB; ++b)
                 if (l0 + b < Lc)
-                    store_tile<G, false, false, IL>(layer_rows(l0 + b), s_idx, regs[b], s_cs, 0,
-                                                s_ident, none);
+                    store_tile<G, false, false, IL, kPack>(layer_rows(l0 + b), s_idx, regs[b],
+                                                           s_cs, 0, s_ident, none);
         }
         return;
     }

@@ -71,10 +71,12 @@ using GeoMhaInPlace = Geo<kInPlaceTileMha, 512, 32, 8, 4>;
 // Multi-head rows (GQA, MHA: rotation is half of every row) without a
 // patch term, in rotate-half pairing, take the pair-packed rotation; the
 // others (MLA's single 64-wide head, patched or interleaved rows) keep one
-// (c1, c2, s1, s2) entry per frequency.
-template <class G, bool PATCH, bool IL>
+// (c1, c2, s1, s2) entry per frequency -- except in passes that move only
+// the rotary part (ROT_ONLY), where the rotation is all the work and MLA
+// rows take the pair-packed rotation too.
+template <class G, bool PATCH, bool IL, bool ROT_ONLY = false>
 struct CsOrder {
-    static constexpr bool kPacked = !PATCH && !IL && G::NH > 1;
+    static constexpr bool kPacked = !PATCH && !IL && (G::NH > 1 || ROT_ONLY);
 };
 
 // Write table entry q of frequency f into a shared-memory cos/sin row.
@@ -258,7 +260,8 @@ __device__ __forceinline__ uint4 rotate_vec_il(uint4 x, const float4 *cs_row, in
 // cs + row*cs_row_stride, see Geo::cs_index) unless the row is marked
 // identity.
 // IL: the rotary pairs are interleaved (x[2j], x[2j+1]) instead of rotate-half.
-template <class G, bool PATCH, bool COPY = true, bool IL = false>
+template <class G, bool PATCH, bool COPY = true, bool IL = false,
+          bool PACKED = CsOrder<G, PATCH, IL>::kPacked>
 __device__ __forceinline__ void store_tile(const RowsAt &at, const int64_t *idx,
                                            const TileRegs<G> &regs, const float4 *cs,
                                            int cs_row_stride, const int32_t *ident,
@@ -308,7 +311,7 @@ __device__ __forceinline__ void store_tile(const RowsAt &at, const int64_t *idx,
                     out = patched ? add_vec(regs.r[k], add) : regs.r[k];
                 else if (IL)
                     out = rotate_vec_il<G>(regs.r[k], cs + row * cs_row_stride, v, add);
-                else if (CsOrder<G, PATCH, IL>::kPacked)
+                else if (PACKED)
                     out = rotate_vec_packed(regs.r[k], partner, first,
                                             cs + row * cs_row_stride + fb / 8, G::HV);
                 else

@@ -154,14 +154,22 @@ __global__ void __launch_bounds__(kSpliceThreads, kSpliceMinBlocks) splice_kerne
                     s_dep[n++] = j;
         }
     }
-    for (int j = tid; j < G::kHalf; j += kThreads)
-        stage_cs<G, CsOrder<G, false, IL>::kPacked>(
-            s_cs, j, p.inline_table ? delta_entry_call(S.delta, j, 2 * G::kHalf, p.rope_base)
-                                    : p.table[(int64_t)q * G::kHalf + j]);
+    if (!p.inline_table)
+        for (int j = tid; j < G::kHalf; j += kThreads)
+            stage_cs<G, CsOrder<G, false, IL>::kPacked>(s_cs, j,
+                                                     p.table[(int64_t)q * G::kHalf + j]);
     __syncthreads();
 
     if (tid >= kThreads) {
-        // the publishing warp: this unit's read counter, once per layer
+        // the publishing warp: a launch without a δ table has it form this
+        // unit's cos/sin rows (fp64 angle reduction) while the row-moving
+        // warps' first loads are in flight -- the rows reach shared memory
+        // before the first layer's barrier, which the stores wait for --
+        // then this unit's read counter, once per layer
+        if (p.inline_table && shift)
+            for (int j = tid - kThreads; j < G::kHalf; j += 32)
+                stage_cs<G, CsOrder<G, false, IL>::kPacked>(
+                    s_cs, j, delta_entry_call(S.delta, j, 2 * G::kHalf, p.rope_base));
         uint32_t *flag = shift && t != p.skip_publish ? p.flags + S.flag_base + k * NG + g
                                                        : nullptr;
         for (int l = l0; l < l1; ++l)

@@ -57,7 +57,8 @@ inline int tile_rows(RowKind kind)
 
 // Rows per tile of the in-place passes over multi-head rows (the ticketed
 // splice, the composed splice and the block-table remap): half the rows of
-// the relocation's tiles, at four blocks per SM.
+// the relocation's tiles, at three (splices: 288-thread blocks) or four
+// (remap) blocks per SM.
 constexpr int kInPlaceTileGqa = 8;
 constexpr int kInPlaceTileGqa4 = 16;
 constexpr int kInPlaceTileMha = 2;

@@ -98,6 +98,7 @@ KERNEL_SOURCES = {
     "window_gqa": ("kv_splice.cu", "kv_patch_tc.cu", "kv_api.cu") + _DEVICE_SOURCES,
     "cdc_tokens": ("kv_cdc.cu", "kv_device.cuh", "kv_internal.h"),
     "families": ("kv_relocate.cu",) + _DEVICE_SOURCES,
+    "sweep_mla": ("kv_relocate.cu",) + _DEVICE_SOURCES,
 }
 
 
@@ -1711,8 +1712,9 @@ def run_window_gqa(args, rank, world, local):
 SWEEP_MLA = dict(layers=61, chunk_lens=(16, 64, 256, 1024, 4096),
                  deltas=(1, -1, 1000, -1000, 100000, -100000), num_reqs=8, req_tokens=131072,
                  rank=8, base=10000.0, splice_seq=131072)
-# A small case of the same kernels (~1 GB on the device).
-SWEEP_MLA_SMALL = dict(SWEEP_MLA, layers=4, num_reqs=2, req_tokens=16384,
+# A small case of the same kernels for counter captures: 16 layers x 4 x 16,384
+# tokens, 2.4 GB moved per relocation call (19x the L2), a few GB on the device.
+SWEEP_MLA_SMALL = dict(SWEEP_MLA, layers=16, num_reqs=4, req_tokens=16384,
                        deltas=(1, -1, 1000, -1000, 10000, -10000), splice_seq=16384)
 
 
@@ -1968,7 +1970,8 @@ def run_sweep_mla(args, rank, world, local):
                    "relocate": reloc, "splice": splice, "patch": patch,
                    "l2": "relocation and patch move >= 4 GB per call; splice points say"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind, "traffic": None,
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": recorded_traffic("sweep_mla"),
                      "kernel": "relocate_kernel<MLA> over all sweep points",
                      "kernel_ms": tot_kms / len(reloc),
                      "algorithmic_bytes_per_launch": tot_bytes / len(reloc)},
